@@ -1,0 +1,129 @@
+/*
+ * kps.h — C ABI of the GB300 (sm_103a) decode-step token sampler.
+ *
+ * One call runs the whole per-step sampling post-process over a [B, V]
+ * logits matrix, row by row:
+ *
+ *   1. repetition penalty over the row's seen ids
+ *        x = x > 0 ? x / penalty : x * penalty, once per distinct id
+ *        (MiniMind "Chapter 10: inference generation", §10.7; the C++
+ *        post-processing blog, repetition_penalty section);
+ *   2. temperature: x = x / temperature (MiniMind ch.10, §10.4);
+ *   3. top-k: keep exactly the first k elements in the order "value
+ *        descending, index ascending" when 1 <= k <= min(V, 1024), skip the
+ *        stage otherwise (Ascend "torch_npu.npu_top_k_top_p_sample", topK
+ *        item 2; MiniMind ch.10, §10.5);
+ *   4. top-p: keep the shortest prefix of that order whose softmax mass
+ *        reaches top_p (at least one element; top_p <= 0 keeps one element,
+ *        top_p >= 1 or NaN skips the stage) (Ascend page, topP full-sort
+ *        formula; MiniMind ch.10, §10.6);
+ *   5. exponential race: index = argmax over the kept set of
+ *        softmax(filtered) / (q + eps), lower index on an exact tie
+ *        (Ascend page, "Sample" formulas).
+ *
+ * It writes the chosen index per row and, when need_logits is set, the
+ * filtered logits in vocabulary order: the transformed value at kept
+ * positions and -inf elsewhere (Ascend page, logits_top_kp_select).
+ *
+ * Value conventions (readings where the pages are silent):
+ *   - NaN logits are treated as -inf;
+ *   - a row whose temperature is not finite and > 0 is greedy: no division,
+ *     only the best (penalised) element is kept and chosen;
+ *   - a penalty <= 0 or NaN disables the penalty for that row; seen ids
+ *     outside [0, V) are ignored; duplicate ids are applied once;
+ *   - softmax weights are exp(x - max) with weight 1 at the maximum itself;
+ *   - race scores that are NaN are ignored; if every score is NaN the first
+ *     element of the order is chosen.
+ *
+ * Memory: every pointer argument of kps_sample is a DEVICE pointer owned by
+ * the caller.  The library allocates nothing, keeps no per-call state and
+ * never synchronises the stream.  Calls on different streams are
+ * independent provided they use different workspaces and outputs.
+ *
+ * Errors: argument checks run on the host before anything is launched and
+ * return a status code.  A launch failure returns KPS_ERR_CUDA.  Faults the
+ * kernel detects itself (a bounded wait that ran out) are recorded in the
+ * workspace status word; read them with kps_last_device_status().
+ */
+#ifndef KPS_H_
+#define KPS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { KPS_F32 = 0, KPS_BF16 = 1 } kps_dtype;
+
+typedef enum {
+  KPS_OK = 0,
+  KPS_ERR_INVALID_ARG = 1,  /* null pointer, bad size, bad dtype, bad eps      */
+  KPS_ERR_UNSUPPORTED = 2,  /* V too large for the on-chip row layout          */
+  KPS_ERR_WORKSPACE = 3,    /* workspace missing, misaligned or too small      */
+  KPS_ERR_CUDA = 4,         /* a CUDA runtime call or the launch failed        */
+  KPS_ERR_TIMEOUT = 5       /* device side: a bounded wait ran out             */
+} kps_status;
+
+/* Bytes of device workspace kps_sample needs for a [B, V] call of dtype dt
+ * (256-byte aligned start required).  The workspace holds the device status
+ * word; zero it once before first use (kps_last_device_status also clears
+ * it).  Returns 0 for invalid sizes. */
+size_t kps_workspace_size(int64_t B, int64_t V, kps_dtype dt);
+
+/* Largest vocabulary size kps_sample accepts for dtype dt on the current
+ * device (the whole row must fit in the shared memory of one thread-block
+ * cluster). */
+int64_t kps_max_vocab(kps_dtype dt);
+
+/*
+ * kps_sample — the fused sampling step (see the file comment for the math).
+ *
+ *   logits        [B, V] row-major, fp32 or bf16 (dt), read only.
+ *   top_k         [B] int32.  Stage active iff 1 <= top_k[b] <= min(V, 1024).
+ *   top_p         [B] fp32.
+ *   temperature   [B] fp32.
+ *   seen_indptr   [B+1] int32 CSR row pointer into seen_ids, or NULL.
+ *   seen_ids      [nnz] int32 token ids already generated per row, or NULL.
+ *   penalty       [B] fp32 repetition penalty, or NULL.  The penalty stage
+ *                 runs only when all three of seen_indptr, seen_ids and
+ *                 penalty are non-NULL.
+ *   q             [B, V] fp32 race weights (Exp(1) draws supplied by the
+ *                 caller).  Required.
+ *   eps           added to q before dividing; must be >= 0 and finite.
+ *   need_logits   non-zero: write out_filtered.
+ *   out_idx       [B] int64 chosen token per row.
+ *   out_filtered  [B, V] fp32; required iff need_logits.
+ *   workspace     device buffer of at least kps_workspace_size(B, V, dt)
+ *                 bytes, 256-byte aligned.
+ *   stream        CUDA stream the work is queued on (0 = legacy default).
+ *
+ * B == 0 is a valid no-op.  Returns KPS_OK once the work is queued.
+ */
+kps_status kps_sample(const void* logits, kps_dtype dt, int64_t B, int64_t V,
+                      const int32_t* top_k, const float* top_p, const float* temperature,
+                      const int32_t* seen_indptr, const int32_t* seen_ids,
+                      const float* penalty, const float* q, float eps, int need_logits,
+                      int64_t* out_idx, float* out_filtered,
+                      void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Reads (and clears) the device status word of a workspace: waits for the
+ * stream, stores KPS_OK or the first device-side error code in *out. */
+kps_status kps_last_device_status(void* workspace, cudaStream_t stream, int* out);
+
+/* Static description of a status code. */
+const char* kps_status_string(kps_status s);
+
+/* Launch shape kps_sample would use for (B, V, dt) on the current device:
+ * cluster size (CTAs per row), elements per CTA, dynamic shared memory per
+ * CTA in bytes.  Returns KPS_OK or an error for unsupported sizes. */
+kps_status kps_query_launch(int64_t B, int64_t V, kps_dtype dt, int* cluster_size,
+                            int64_t* chunk_elems, size_t* smem_bytes);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KPS_H_ */

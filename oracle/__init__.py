@@ -1,0 +1,92 @@
+"""CPU oracle for the decode-step sampling post-process — TEST INFRASTRUCTURE ONLY.
+
+The oracle is a plain single-threaded C++ implementation (kps_oracle.cpp)
+written from the method's definition.  Only the tests, the smoke check and the
+benchmark's CPU-baseline leg may import this package; the product path never
+does.  It shares no code with the CUDA library.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kps_oracle.cpp")
+_LIB = os.path.join(_HERE, "libkps_oracle.so")
+_lib: Optional[ctypes.CDLL] = None
+
+# -ffp-contract=off: every fp32 step is a single IEEE operation (no fused
+# multiply-add contraction), matching the definition.
+CXXFLAGS = ["-O2", "-std=c++17", "-shared", "-fPIC", "-ffp-contract=off", "-fno-fast-math"]
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle shared library in-tree (seconds); returns its path."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["g++", *CXXFLAGS, "-o", tmp, _SRC])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB)
+        P = ctypes.c_void_p
+        lib.kpso_sample.restype = ctypes.c_int
+        lib.kpso_sample.argtypes = [P, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, P, P, P, P, P, P,
+                                    P, ctypes.c_float, ctypes.c_int, P, P, P, P, P]
+        _lib = lib
+    return _lib
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def sample_arrays(logits: np.ndarray, dtype: str, top_k, top_p, temperature, q, eps: float = 1e-20,
+                  need_logits: bool = True, seen_indptr=None, seen_ids=None, penalty=None) -> dict:
+    """Run the oracle on host arrays.  logits: float32 [B,V] or uint16 bf16 bits [B,V]."""
+    lib = _load()
+    if dtype == "f32":
+        logits = np.ascontiguousarray(logits, dtype=np.float32)
+    elif dtype == "bf16":
+        logits = np.ascontiguousarray(logits, dtype=np.uint16)
+    else:
+        raise ValueError(dtype)
+    B, V = logits.shape
+    top_k = np.ascontiguousarray(top_k, dtype=np.int32)
+    top_p = np.ascontiguousarray(top_p, dtype=np.float32)
+    temperature = np.ascontiguousarray(temperature, dtype=np.float32)
+    q = np.ascontiguousarray(q, dtype=np.float32)
+    assert q.shape == (B, V) and top_k.shape == (B,) and top_p.shape == (B,) and temperature.shape == (B,)
+    if seen_indptr is not None:
+        seen_indptr = np.ascontiguousarray(seen_indptr, dtype=np.int32)
+        seen_ids = np.ascontiguousarray(seen_ids, dtype=np.int32)
+        penalty = np.ascontiguousarray(penalty, dtype=np.float32)
+    out_idx = np.empty(B, dtype=np.int64)
+    out = np.empty((B, V), dtype=np.float32) if need_logits else None
+    kept = np.empty(B, dtype=np.int64)
+    race_gap = np.empty(B, dtype=np.float64)
+    topp_gap = np.empty(B, dtype=np.float64)
+    rc = lib.kpso_sample(_ptr(logits), 0 if dtype == "f32" else 1, B, V, _ptr(top_k), _ptr(top_p),
+                         _ptr(temperature), _ptr(seen_indptr), _ptr(seen_ids), _ptr(penalty), _ptr(q),
+                         float(eps), 1 if need_logits else 0, _ptr(out_idx), _ptr(out), _ptr(kept),
+                         _ptr(race_gap), _ptr(topp_gap))
+    if rc != 0:
+        raise ValueError(f"oracle rejected its arguments (code {rc})")
+    return dict(idx=out_idx, filtered=out, kept=kept, race_gap=race_gap, topp_gap=topp_gap)
+
+
+def sample(inp, need_logits: Optional[bool] = None) -> dict:
+    """Run the oracle on a workloads.SamplingInputs."""
+    nl = inp.need_logits if need_logits is None else need_logits
+    return sample_arrays(inp.logits, inp.dtype, inp.top_k, inp.top_p, inp.temperature, inp.q, inp.eps,
+                         nl, inp.seen_indptr, inp.seen_ids, inp.penalty)

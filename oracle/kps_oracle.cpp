@@ -1,0 +1,220 @@
+// kps_oracle.cpp — plain, slow, single-threaded CPU oracle for the per-step
+// token-sampling post-process (repetition penalty -> temperature -> top-k ->
+// top-p -> exponential race).
+//
+// TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or load
+// this file: only the tests, the smoke check and the benchmark's CPU-baseline
+// leg use it.  It shares no code, header or constant with the CUDA library.
+//
+// Sources (the three pages this method is described on):
+//   [NPU]  Ascend API reference "torch_npu.npu_top_k_top_p_sample":
+//          topK item 2 (valid range 1 <= k <= min(V,1024), otherwise skip),
+//          the topP full-sort fallback (sort desc, cumsum, drop where the
+//          exclusive cumsum exceeds top_p), and the Sample formula
+//          (probs = softmax(filtered); idx = argmax(probs / (q + eps))).
+//   [MM10] MiniMind "Chapter 10: inference generation": §10.4 temperature
+//          (logits / T), §10.5 top-k threshold mask, §10.6 top-p via sorted
+//          softmax cumsum with the mask shifted right by one, §10.7 repetition
+//          penalty (score > 0 ? score / p : score * p over the unique seen ids).
+//   [CPP]  "LLM sampling post-processing summary: the C++ implementation":
+//          repetition_penalty over a set of ids (duplicates applied once),
+//          softmax (max, exp, sum) and the top_p rule "smallest set whose
+//          mass reaches top_p".
+//
+// Readings fixed where the pages are silent or disagree (each one is listed
+// with its reason in the design notes):
+//   * penalty first, then temperature; both are IEEE fp32 operations
+//     (x / p, x * p, x / T), exactly as the GPU performs them;
+//   * NaN logits become -inf before anything else;
+//   * a row whose temperature is not a finite positive number is greedy:
+//     no division, the kept set is the single best element;
+//   * penalty <= 0 or NaN skips the penalty for that row; seen ids outside
+//     [0, V) are ignored;
+//   * total order "pi": value descending, then index ascending;
+//   * top-k keeps exactly the first k elements under pi when
+//     1 <= k <= min(V, 1024) and is the identity otherwise [NPU topK item 2];
+//   * softmax over the top-k set in double with e_v = exp(x_v - M); an element
+//     equal to the maximum M gets weight exactly 1 (so +-inf maxima are finite);
+//   * top-p keeps the shortest pi-prefix whose mass reaches p * S: an element
+//     is kept while the exclusive prefix mass is < p * S [MM10 §10.6 worked
+//     example keeps the token that first reaches the threshold]; p <= 0 keeps
+//     one element, p >= 1 or NaN skips the stage;
+//   * race: r_v = (e_v / S_P) / (q_v + eps) in double over the kept set P,
+//     argmax with the lower index winning an exact tie, NaN scores ignored,
+//     the pi-first element if every score is NaN;
+//   * filtered output: the transformed value at kept positions, -inf elsewhere.
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <limits>
+#include <vector>
+
+namespace {
+
+float bf16_bits_to_float(uint16_t h) {
+  uint32_t u = static_cast<uint32_t>(h) << 16;
+  float f;
+  std::memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+// One row of the method, written out step by step.
+struct RowResult {
+  int64_t idx;
+  int64_t kept;
+  double race_gap;  // (best - second best) / best race score, +inf if < 2 scores
+  double topp_gap;  // distance of the deciding cumsums from p*S, relative to p*S
+};
+
+RowResult sample_row(std::vector<float>& x, int64_t V, int32_t k, float p, float T,
+                     const int32_t* ids, int64_t nids, bool pen_on, float pen,
+                     const float* qrow, float eps, float* out_row) {
+  const float NEG_INF = -std::numeric_limits<float>::infinity();
+
+  // NaN logits are treated as -inf.
+  for (int64_t v = 0; v < V; ++v)
+    if (std::isnan(x[v])) x[v] = NEG_INF;
+
+  // Repetition penalty over the SET of seen ids [MM10 §10.7, CPP repetition_penalty].
+  if (pen_on) {
+    std::vector<char> seen(static_cast<size_t>(V), 0);
+    for (int64_t j = 0; j < nids; ++j) {
+      int64_t id = ids[j];
+      if (id < 0 || id >= V || seen[id]) continue;
+      seen[id] = 1;
+      float s = x[id];
+      x[id] = (s > 0.0f) ? (s / pen) : (s * pen);
+    }
+  }
+
+  // Temperature [MM10 §10.4]: x / T, or greedy when T is not finite and positive.
+  const bool greedy = !(T > 0.0f) || std::isinf(T);
+  if (!greedy)
+    for (int64_t v = 0; v < V; ++v) x[v] = x[v] / T;
+
+  // Total order pi: value descending, index ascending.
+  auto before = [&x](int64_t a, int64_t b) {
+    return x[a] > x[b] || (x[a] == x[b] && a < b);
+  };
+  std::vector<int64_t> order(static_cast<size_t>(V));
+  for (int64_t v = 0; v < V; ++v) order[v] = v;
+
+  // Top-k [NPU topK item 2; MM10 §10.5]: exactly the first k under pi.
+  const bool topk_on = (k >= 1) && (static_cast<int64_t>(k) <= std::min<int64_t>(V, 1024));
+  int64_t nK = V;
+  if (topk_on) {
+    nK = k;
+    std::nth_element(order.begin(), order.begin() + (nK - 1), order.end(), before);
+    std::sort(order.begin(), order.begin() + nK, before);
+  } else {
+    std::sort(order.begin(), order.end(), before);
+  }
+
+  // Softmax over K in double [CPP softmax; NPU topK softmax step].
+  const double M = static_cast<double>(x[order[0]]);
+  std::vector<double> e(static_cast<size_t>(nK));
+  double S = 0.0;
+  for (int64_t i = 0; i < nK; ++i) {
+    double xv = static_cast<double>(x[order[i]]);
+    e[i] = (xv == M) ? 1.0 : std::exp(xv - M);
+    S += e[i];
+  }
+
+  // Top-p [NPU topP fallback; MM10 §10.6; CPP top_p].
+  int64_t nP = nK;
+  double topp_gap = std::numeric_limits<double>::infinity();
+  if (greedy || p <= 0.0f) {
+    nP = 1;
+  } else if (p < 1.0f) {
+    const double target = static_cast<double>(p) * S;
+    double c = 0.0, c_before_last = 0.0;
+    nP = 0;
+    while (nP < nK && c < target) {
+      c_before_last = c;
+      c += e[nP];
+      ++nP;
+    }
+    double lo = target - c_before_last;  // > 0: the last kept element was needed
+    double hi = c - target;              // >= 0: the prefix reaches the target
+    topp_gap = std::min(std::fabs(lo), std::fabs(hi)) / target;
+  }
+
+  // Exponential race [NPU Sample]: argmax of (e / S_P) / (q + eps).
+  double SP = 0.0;
+  for (int64_t i = 0; i < nP; ++i) SP += e[i];
+  int64_t best = -1;
+  double rbest = 0.0, rsecond = -std::numeric_limits<double>::infinity();
+  for (int64_t i = 0; i < nP; ++i) {
+    int64_t v = order[i];
+    double r = (e[i] / SP) / (static_cast<double>(qrow[v]) + static_cast<double>(eps));
+    if (std::isnan(r)) continue;
+    if (best < 0 || r > rbest || (r == rbest && v < best)) {
+      if (best >= 0) rsecond = std::max(rsecond, rbest);
+      best = v;
+      rbest = r;
+    } else {
+      rsecond = std::max(rsecond, r);
+    }
+  }
+  if (best < 0) best = order[0];
+  double race_gap = std::numeric_limits<double>::infinity();
+  if (nP >= 2 && std::isfinite(rsecond) && rbest != 0.0)
+    race_gap = (rbest - rsecond) / std::fabs(rbest);
+
+  // Filtered logits [NPU Sample, logits_top_kp_select]: kept values, -inf elsewhere.
+  if (out_row) {
+    for (int64_t v = 0; v < V; ++v) out_row[v] = NEG_INF;
+    for (int64_t i = 0; i < nP; ++i) out_row[order[i]] = x[order[i]];
+  }
+  return RowResult{best, nP, race_gap, topp_gap};
+}
+
+}  // namespace
+
+extern "C" {
+
+// Returns 0 on success, 1 on an invalid argument.  dtype: 0 = fp32, 1 = bf16.
+// seen_indptr / seen_ids / penalty may all be NULL (no penalty).
+// out_filtered may be NULL when need_logits == 0.  The three diagnostic
+// outputs (kept count, race gap, top-p gap per row) may be NULL.
+int kpso_sample(const void* logits, int dtype, int64_t B, int64_t V,
+                const int32_t* top_k, const float* top_p, const float* temperature,
+                const int32_t* seen_indptr, const int32_t* seen_ids, const float* penalty,
+                const float* q, float eps, int need_logits,
+                int64_t* out_idx, float* out_filtered,
+                int64_t* out_kept, double* out_race_gap, double* out_topp_gap) {
+  if (B < 0 || V < 1 || !logits || !top_k || !top_p || !temperature || !q || !out_idx)
+    return 1;
+  if (dtype != 0 && dtype != 1) return 1;
+  if (need_logits && !out_filtered) return 1;
+  std::vector<float> x(static_cast<size_t>(V));
+  for (int64_t b = 0; b < B; ++b) {
+    if (dtype == 0) {
+      const float* row = static_cast<const float*>(logits) + b * V;
+      for (int64_t v = 0; v < V; ++v) x[v] = row[v];
+    } else {
+      const uint16_t* row = static_cast<const uint16_t*>(logits) + b * V;
+      for (int64_t v = 0; v < V; ++v) x[v] = bf16_bits_to_float(row[v]);
+    }
+    bool pen_on = seen_indptr && seen_ids && penalty && (penalty[b] > 0.0f);
+    const int32_t* ids = nullptr;
+    int64_t nids = 0;
+    if (pen_on) {
+      ids = seen_ids + seen_indptr[b];
+      nids = static_cast<int64_t>(seen_indptr[b + 1]) - seen_indptr[b];
+      if (nids < 0) nids = 0;
+    }
+    RowResult r = sample_row(x, V, top_k[b], top_p[b], temperature[b], ids, nids, pen_on,
+                             pen_on ? penalty[b] : 1.0f, q + b * V, eps,
+                             need_logits ? out_filtered + b * V : nullptr);
+    out_idx[b] = r.idx;
+    if (out_kept) out_kept[b] = r.kept;
+    if (out_race_gap) out_race_gap[b] = r.race_gap;
+    if (out_topp_gap) out_topp_gap[b] = r.topp_gap;
+  }
+  return 0;
+}
+
+}  // extern "C"
