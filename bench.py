@@ -1,0 +1,391 @@
+#!/usr/bin/env python3
+"""Throughput benchmark of the fused decode-step sampler on GB300.
+
+Default workload (one step = one kps_sample call over the whole batch):
+  batch256_penalty: B=256, V=151936, fp32 logits, per-row top-k (10% skipped),
+  top-p, temperature, repetition penalty over 512 seen ids, q ~ Exp(1),
+  filtered logits written.
+
+Prints ONE JSON line.  value = sampled rows/s over all ranks (one token per
+row).  The inputs (logits + q + filtered output = 467 MB) are larger than the
+129 MB L2, so no flush is needed between timed steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   (the CPU oracle on host cores)
+
+Under torchrun (N > 1) every rank runs its own full batch (rows are
+independent; no collective on the data path) and the slowest rank's time is
+reported: weak scaling.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+NOMINAL_HBM_GBS = 8000.0
+KERNEL_NAME = "kps_sample_kernel"
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=float(d["hbm_gbs"]), source="measured")
+    return dict(hbm_gbs=6800.0, source="fallback")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in ("decode_token_sampling_gb300/csrc/kps.cu", "include/kps.h"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic_per_launch(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this kernel source."""
+    p = os.path.join(ROOT, "profiles", f"kps_sample_kernel_{workload}.md")
+    if not os.path.exists(p):
+        return None
+    txt = open(p).read()
+    m_hash = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", txt)
+    m_b = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", txt)
+    if not m_hash or not m_b or m_hash.group(1) != kernel_source_hash():
+        return None
+    return int(m_b.group(1))
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", str(self.gpu)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_reference(args, ws, rank):
+    """The CPU oracle, timed on the host cores over a bounded sample of the workload's rows."""
+    if rank != 0:
+        return 0
+    import oracle
+    from decode_token_sampling_gb300.workloads import make_workload
+    oracle.build()
+    # bounded sample: about a minute of oracle work in total whatever --steps is
+    n_rows = max(1, min(args.ref_rows, 12000 // max(args.steps, 1)))
+    rows = list(range(n_rows))
+    inp = make_workload(args.workload, rows=rows)
+    for _ in range(max(0, min(args.warmup, 1))):
+        oracle.sample(inp)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.sample(inp)
+        times.append(time.perf_counter() - t0)
+    t = sum(times)
+    rows_per_s = len(rows) * args.steps / t
+    sample = f"first {len(rows)} rows of {args.workload} per step, {args.steps} steps"
+    line = {
+        "impl": "reference", "metric": metric_name(args.workload), "value": rows_per_s, "unit": "rows/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(args.workload),
+        "cpu_baseline": {"value": rows_per_s, "unit": "rows/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": rows_per_s, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def metric_name(workload: str) -> str:
+    return "sampled rows/s (= sampled tokens/s) of the fused penalty/temperature/top-k/top-p/race step" \
+           if workload == "batch256_penalty" else f"sampled rows/s ({workload})"
+
+
+def workload_config(workload: str) -> dict:
+    from decode_token_sampling_gb300.workloads import make_workload
+    desc = {
+        "batch256_penalty": dict(B=256, V=151936, logits="fp32", need_logits=True,
+                                 top_k="U[1,1024], 10% skipped", top_p="U[0.5,1.0]", temperature="U[0.5,1.2]",
+                                 penalty="1.1 over 512 seen ids/row"),
+        "flat_nucleus": dict(B=128, V=151936, logits="fp32", need_logits=False, top_k="skip",
+                             top_p="U[0.95,0.999]", temperature=1.0),
+        "bf16_zipf": dict(B=64, V=128256, logits="bf16", need_logits=False),
+        "small_mixed": dict(B=4, V=32000, logits="fp32", need_logits=True),
+        "single_row_long": dict(B=1, V=262144, logits="bf16", need_logits=False),
+    }[workload]
+    return {"workload": workload, **desc,
+            "l2": "no flush: logits+q(+out) per step exceed the 129 MB L2" if workload in
+            ("batch256_penalty", "flat_nucleus") else "inputs smaller than L2 (latency workload)"}
+
+
+def cpu_baseline(args) -> dict:
+    import oracle
+    from decode_token_sampling_gb300.workloads import make_workload
+    oracle.build()
+    rows = list(range(args.ref_rows))
+    inp = make_workload(args.workload, rows=rows)
+    reps = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.sample(inp)
+        reps += 1
+        if time.perf_counter() - t0 > args.cpu_seconds:
+            break
+    t = time.perf_counter() - t0
+    return {"value": reps * len(rows) / t, "unit": "rows/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {len(rows)} rows of {args.workload}, repeated {reps}x ({t:.1f} s, single thread)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="kps", choices=["kps", "reference"])
+    ap.add_argument("--workload", default="batch256_penalty")
+    ap.add_argument("--ref-rows", type=int, default=16)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, ws, rank)
+
+    import numpy as np
+    import torch
+    import decode_token_sampling_gb300 as kps
+    from decode_token_sampling_gb300 import build as kbuild
+    from decode_token_sampling_gb300.workloads import make_workload
+
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    kbuild.build()
+
+    inp = make_workload(args.workload)
+    B, V = inp.B, inp.V
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    if inp.dtype == "bf16":
+        logits = t(inp.logits.view(np.int16)).view(torch.bfloat16)
+    else:
+        logits = t(inp.logits)
+    top_k, top_p, temp, q = t(inp.top_k), t(inp.top_p), t(inp.temperature), t(inp.q)
+    pen_kw = {}
+    if inp.seen_indptr is not None:
+        pen_kw = dict(seen_indptr=t(inp.seen_indptr), seen_ids=t(inp.seen_ids), penalty=t(inp.penalty))
+    out_idx = torch.empty(B, dtype=torch.int64, device=dev)
+    out_f = torch.empty(B, V, dtype=torch.float32, device=dev) if inp.need_logits else None
+    wsp = kps.new_workspace(B, V, logits.dtype, dev)
+    stream = torch.cuda.Stream(dev)
+
+    def step():
+        kps.sample(logits, top_k, top_p, temp, q, eps=inp.eps, need_logits=inp.need_logits, out_idx=out_idx,
+                   out_filtered=out_f, workspace=wsp, stream=stream, **pen_kw)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    stream.synchronize()
+
+    # ---- device-resident timed region --------------------------------------------------------
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t_all0 = torch.cuda.Event(enable_timing=True)
+    t_all1 = torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(dev.index if ws == 1 else local)
+    clocks.start()
+    time.sleep(0.3)  # let the sampler come up
+    t_all0.record(stream)
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    t_all1.record(stream)
+    torch.cuda.synchronize(dev)
+    if ws > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    total_ms = t_all0.elapsed_time(t_all1)
+    per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    kernel_ms = sum(per_launch_ms) / len(per_launch_ms)
+    if ws > 1:
+        tt = torch.tensor([total_ms, kernel_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        total_ms, kernel_ms = tt.tolist()
+    ms_per_step = total_ms / args.steps
+    rows_per_s = ws * B * args.steps / (total_ms / 1e3)
+
+    status = kps.last_device_status(wsp, stream)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+
+    # ---- algorithmic bytes of one launch ----------------------------------------------------
+    esize = 4 if inp.dtype == "f32" else 2
+    if out_f is not None:
+        kept = (out_f != float("-inf")).sum(dim=1).to(torch.int64)
+    else:
+        _, f_tmp = kps.sample(logits, top_k, top_p, temp, q, eps=inp.eps, need_logits=True, workspace=wsp, **pen_kw)
+        kept = (f_tmp != float("-inf")).sum(dim=1).to(torch.int64)
+        del f_tmp
+    nnz = int(inp.seen_ids.size) if inp.seen_ids is not None else 0
+    alg_bytes = (B * V * esize + (B * V * 4 if inp.need_logits else 0) + int(kept.sum().item()) * 4 + nnz * 4
+                 + B * (4 * 4 + 8 + (4 if pen_kw else 0)))
+    metric_bytes = inp.metric_bytes()
+    peaks = measured_peaks()
+    achieved_gbs = alg_bytes / (kernel_ms / 1e3) / 1e9
+    traffic = ncu_traffic_per_launch(args.workload)
+
+    # ---- end to end through the public API: pinned host inputs in, results out ---------------
+    h = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    h_logits = h(inp.logits if inp.dtype == "f32" else inp.logits.view(np.int16))
+    h_q, h_k, h_p, h_t = h(inp.q), h(inp.top_k), h(inp.top_p), h(inp.temperature)
+    h_pen = {k: h(getattr(inp, k)) for k in ("seen_indptr", "seen_ids", "penalty")} if pen_kw else {}
+    h_idx = torch.empty(B, dtype=torch.int64).pin_memory()
+    h_out = torch.empty(B, V, dtype=torch.float32).pin_memory() if inp.need_logits else None
+    d_logits, d_q = torch.empty_like(logits), torch.empty_like(q)
+    d_k, d_p, d_t = torch.empty_like(top_k), torch.empty_like(top_p), torch.empty_like(temp)
+    d_pen = {k: torch.empty_like(v) for k, v in pen_kw.items()}
+    h2d = sum(x.numel() * x.element_size() for x in [h_logits, h_q, h_k, h_p, h_t, *h_pen.values()])
+    d2h = h_idx.numel() * 8 + (h_out.numel() * 4 if h_out is not None else 0)
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            d_logits.view(torch.int16 if inp.dtype == "bf16" else torch.float32).copy_(h_logits, non_blocking=True)
+            d_q.copy_(h_q, non_blocking=True)
+            d_k.copy_(h_k, non_blocking=True)
+            d_p.copy_(h_p, non_blocking=True)
+            d_t.copy_(h_t, non_blocking=True)
+            for k_, v_ in d_pen.items():
+                v_.copy_(h_pen[k_], non_blocking=True)
+            kps.sample(d_logits, d_k, d_p, d_t, d_q, eps=inp.eps, need_logits=inp.need_logits, out_idx=out_idx,
+                       out_filtered=out_f, workspace=wsp, stream=stream, **d_pen)
+            h_idx.copy_(out_idx, non_blocking=True)
+            if h_out is not None:
+                h_out.copy_(out_f, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        torch.distributed.barrier()
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    stream.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    if ws > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = tt.item()
+    e2e_rows = ws * B / (e2e_ms / 1e3)
+
+    line = {
+        "metric": metric_name(args.workload), "value": rows_per_s, "unit": "rows/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": inp.dtype, "data": "synthetic (seeded, see workloads.py)",
+        "config": workload_config(args.workload),
+        "tokens_per_s": rows_per_s,
+        "metric_gbs": metric_bytes / (ms_per_step / 1e3) / 1e9,
+        "metric_pct_of_8tbs": 100.0 * metric_bytes / (ms_per_step / 1e3) / 1e9 / NOMINAL_HBM_GBS,
+        "metric_bytes_per_step": metric_bytes,
+        "clocks": clk,
+        "e2e": {"value": e2e_rows, "unit": "rows/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps,
+        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": traffic,
+                     "peak_source": peaks["source"], "kernel": KERNEL_NAME,
+                     "algorithmic_bytes_per_launch": alg_bytes, "kernel_ms": kernel_ms},
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

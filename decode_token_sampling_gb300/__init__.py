@@ -1,0 +1,166 @@
+"""GB300-native decode-step token sampling (penalty -> temperature -> top-k -> top-p
+-> exponential race) over a [batch, vocab] logits matrix.
+
+The work runs in hand-written sm_103a CUDA kernels behind the C ABI declared in
+include/kps.h (libkps.so, built in-tree).  This module only marshals torch
+tensors into that ABI; there is no fallback of any kind: if the library is
+missing or the tensors are not on a CUDA device, calls raise.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkps.so")
+
+KPS_F32, KPS_BF16 = 0, 1
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported size", 3: "workspace missing, misaligned or too small",
+          4: "CUDA error", 5: "device wait timed out"}
+
+
+class KpsError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {STATUS.get(code, 'unknown status')} (code {code})")
+        self.code = code
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def load_library() -> ctypes.CDLL:
+    """Load libkps.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it first (python -m decode_token_sampling_gb300.build)")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I64, I32, F32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+    lib.kps_workspace_size.restype = ctypes.c_size_t
+    lib.kps_workspace_size.argtypes = [I64, I64, I32]
+    lib.kps_max_vocab.restype = I64
+    lib.kps_max_vocab.argtypes = [I32]
+    lib.kps_sample.restype = I32
+    lib.kps_sample.argtypes = [P, I32, I64, I64, P, P, P, P, P, P, P, F32, I32, P, P, P, ctypes.c_size_t, P]
+    lib.kps_last_device_status.restype = I32
+    lib.kps_last_device_status.argtypes = [P, P, ctypes.POINTER(I32)]
+    lib.kps_status_string.restype = ctypes.c_char_p
+    lib.kps_status_string.argtypes = [I32]
+    lib.kps_query_launch.restype = I32
+    lib.kps_query_launch.argtypes = [I64, I64, I32, ctypes.POINTER(I32), ctypes.POINTER(I64),
+                                     ctypes.POINTER(ctypes.c_size_t)]
+    _lib = lib
+    return lib
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return KPS_F32
+    if t.dtype == torch.bfloat16:
+        return KPS_BF16
+    raise TypeError(f"logits must be float32 or bfloat16, got {t.dtype}")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(t: Optional[torch.Tensor], name: str, dtype: torch.dtype, shape: Tuple[int, ...], device) -> None:
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, logits on {device}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def workspace_size(B: int, V: int, dtype: torch.dtype = torch.float32) -> int:
+    code = KPS_BF16 if dtype == torch.bfloat16 else KPS_F32
+    return int(load_library().kps_workspace_size(B, V, code))
+
+
+def new_workspace(B: int, V: int, dtype: torch.dtype = torch.float32, device="cuda") -> torch.Tensor:
+    """A zeroed workspace buffer (uint8) of the size kps_sample needs."""
+    n = max(workspace_size(B, V, dtype), 256)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def query_launch(B: int, V: int, dtype: torch.dtype = torch.float32) -> dict:
+    lib = load_library()
+    cs, nc, sm = ctypes.c_int(0), ctypes.c_int64(0), ctypes.c_size_t(0)
+    code = KPS_BF16 if dtype == torch.bfloat16 else KPS_F32
+    st = lib.kps_query_launch(B, V, code, ctypes.byref(cs), ctypes.byref(nc), ctypes.byref(sm))
+    if st != 0:
+        raise KpsError(st, "kps_query_launch")
+    return dict(cluster_size=cs.value, chunk_elems=nc.value, smem_bytes=sm.value)
+
+
+def sample(logits: torch.Tensor, top_k: torch.Tensor, top_p: torch.Tensor, temperature: torch.Tensor,
+           q: torch.Tensor, *, seen_indptr: Optional[torch.Tensor] = None, seen_ids: Optional[torch.Tensor] = None,
+           penalty: Optional[torch.Tensor] = None, eps: float = 1e-20, need_logits: bool = False,
+           out_idx: Optional[torch.Tensor] = None, out_filtered: Optional[torch.Tensor] = None,
+           workspace: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None):
+    """One fused sampling step on the GPU (asynchronous on `stream`).
+
+    Returns (out_idx int64[B], out_filtered float32[B,V] or None).
+    """
+    lib = load_library()
+    if logits.dim() != 2:
+        raise ValueError("logits must be [B, V]")
+    B, V = logits.shape
+    dev = logits.device
+    if not logits.is_cuda:
+        raise ValueError("logits must be a CUDA tensor")
+    dt = _dtype_code(logits)
+    _check(logits, "logits", logits.dtype, (B, V), dev)
+    _check(top_k, "top_k", torch.int32, (B,), dev)
+    _check(top_p, "top_p", torch.float32, (B,), dev)
+    _check(temperature, "temperature", torch.float32, (B,), dev)
+    _check(q, "q", torch.float32, (B, V), dev)
+    if seen_indptr is not None:
+        _check(seen_indptr, "seen_indptr", torch.int32, (B + 1,), dev)
+        if seen_ids is None or penalty is None:
+            raise ValueError("seen_indptr, seen_ids and penalty go together")
+        _check(seen_ids, "seen_ids", torch.int32, tuple(seen_ids.shape), dev)
+        _check(penalty, "penalty", torch.float32, (B,), dev)
+    if out_idx is None:
+        out_idx = torch.empty(B, dtype=torch.int64, device=dev)
+    _check(out_idx, "out_idx", torch.int64, (B,), dev)
+    if need_logits:
+        if out_filtered is None:
+            out_filtered = torch.empty(B, V, dtype=torch.float32, device=dev)
+        _check(out_filtered, "out_filtered", torch.float32, (B, V), dev)
+    else:
+        out_filtered = None
+    if workspace is None:
+        workspace = new_workspace(B, V, logits.dtype, dev)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    st = lib.kps_sample(_ptr(logits), dt, B, V, _ptr(top_k), _ptr(top_p), _ptr(temperature), _ptr(seen_indptr),
+                        _ptr(seen_ids), _ptr(penalty), _ptr(q), float(eps), 1 if need_logits else 0,
+                        _ptr(out_idx), _ptr(out_filtered), _ptr(workspace), workspace.numel(),
+                        ctypes.c_void_p(s.cuda_stream))
+    if st != 0:
+        raise KpsError(st, "kps_sample")
+    return out_idx, out_filtered
+
+
+def last_device_status(workspace: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> int:
+    """Reads and clears the device status word (0 = ok, 5 = a bounded wait ran out)."""
+    lib = load_library()
+    s = stream if stream is not None else torch.cuda.current_stream(workspace.device)
+    out = ctypes.c_int(0)
+    st = lib.kps_last_device_status(_ptr(workspace), ctypes.c_void_p(s.cuda_stream), ctypes.byref(out))
+    if st != 0:
+        raise KpsError(st, "kps_last_device_status")
+    return out.value

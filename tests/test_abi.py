@@ -1,0 +1,77 @@
+"""CPU-side checks of the C ABI: the library loads, exports every function the
+header declares, and rejects bad arguments on the host before touching a GPU."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from decode_token_sampling_gb300 import build
+    build.build()
+    import decode_token_sampling_gb300 as kps
+    return kps.load_library()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "kps.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kps_[a-z_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_function(lib):
+    names = declared_functions()
+    assert "kps_sample" in names and len(names) >= 6
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_workspace_size(lib):
+    assert lib.kps_workspace_size(256, 151936, 0) >= 4
+    assert lib.kps_workspace_size(-1, 10, 0) == 0
+    assert lib.kps_workspace_size(1, 0, 0) == 0
+    assert lib.kps_workspace_size(1, 10, 7) == 0
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        assert lib.kps_status_string(code)
+
+
+def _call(lib, **over):
+    fake = ctypes.c_void_p(1 << 20)  # never dereferenced: the host checks run first
+    args = dict(logits=fake, dt=0, B=4, V=100, top_k=fake, top_p=fake, temperature=fake, seen_indptr=None,
+                seen_ids=None, penalty=None, q=fake, eps=1e-20, need_logits=0, out_idx=fake, out_filtered=None,
+                workspace=ctypes.c_void_p(1 << 20), workspace_bytes=256, stream=None)
+    args.update(over)
+    return lib.kps_sample(*args.values())
+
+
+def test_host_validation_without_gpu(lib):
+    assert _call(lib, dt=5) == 1
+    assert _call(lib, V=0) == 1
+    assert _call(lib, B=-1) == 1
+    assert _call(lib, eps=-1.0) == 1
+    assert _call(lib, eps=float("nan")) == 1
+    assert _call(lib, eps=float("inf")) == 1
+    assert _call(lib, workspace=None) == 3
+    assert _call(lib, workspace=ctypes.c_void_p((1 << 20) + 8)) == 3
+    assert _call(lib, workspace_bytes=8) == 3
+    assert _call(lib, B=0) == 0  # valid no-op, nothing launched
+    assert _call(lib, logits=None) == 1
+    assert _call(lib, q=None) == 1
+    assert _call(lib, out_idx=None) == 1
+    assert _call(lib, need_logits=1, out_filtered=None) == 1
+
+
+def test_no_silent_cpu_path(lib):
+    """Valid arguments on a machine without a GPU must fail with a CUDA error, never compute."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _call(lib) == 4

@@ -1,0 +1,122 @@
+"""GPU path vs the CPU oracle, element by element, through the C ABI.
+
+Covers the five named workloads at full size (the B=256, V=151936 one in the
+same launch configuration the benchmark times), ragged and tiny vocabularies
+that span several CTAs with ragged tails, heavy ties, NaN/-inf logits,
+penalties with duplicate and out-of-range ids, and the per-row edge cases of
+every stage (top-k out of range, top-p <= 0 / >= 1 / NaN, temperature <= 0 /
+NaN / inf).
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+from decode_token_sampling_gb300.workloads import WORKLOADS, make_random, make_workload
+from parity import compare, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from decode_token_sampling_gb300 import build
+    build.build()
+    oracle.build()
+
+
+@pytest.mark.parametrize("name", WORKLOADS)
+def test_named_workloads(name):
+    inp = make_workload(name)
+    ref = oracle.sample(inp)
+    gi, gf = run_gpu(inp)
+    compare(inp, ref, gi, gf, name)
+    if not inp.need_logits:  # also check the filtered output of the same workload
+        ref = oracle.sample(inp, need_logits=True)
+        gi, gf = run_gpu(inp, need_logits=True)
+        compare(inp, ref, gi, gf, name + "+logits")
+
+
+@pytest.mark.parametrize("V", [1, 2, 7, 31, 33, 1023, 1025, 4099, 8191, 40000])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_ragged_vocab(V, dtype):
+    inp = make_random(6, V, seed=V, dtype=dtype, penalty=1.3, n_seen=min(3 * V, 200))
+    ref = oracle.sample(inp)
+    gi, gf = run_gpu(inp)
+    compare(inp, ref, gi, gf, f"V={V} {dtype}")
+
+
+@pytest.mark.parametrize("V", [64, 5000, 70001])
+def test_ties_and_specials(V):
+    inp = make_random(12, V, seed=7 + V, ties=True, special=True, penalty=1.5, n_seen=50)
+    ref = oracle.sample(inp)
+    gi, gf = run_gpu(inp)
+    compare(inp, ref, gi, gf, f"ties V={V}")
+
+
+def test_all_equal_rows_split_ties_by_index():
+    inp = make_random(8, 3000, seed=11)
+    inp.logits[:] = 0.5
+    inp.top_k[:] = [1, 2, 17, 1024, 0, 0, 700, 3000][:8]
+    inp.top_p[:] = [1.0, 0.5, 1.0, 0.25, 0.5, 0.125, 0.99, 1.0]
+    inp.temperature[:] = 1.0
+    ref = oracle.sample(inp)
+    gi, gf = run_gpu(inp)
+    compare(inp, ref, gi, gf, "all-equal")
+
+
+def test_edge_parameters():
+    B, V = 16, 3001
+    inp = make_random(B, V, seed=99, penalty=1.2, n_seen=40)
+    inp.top_k[:] = [0, -1, 1, 1024, 1025, V, V + 7, 5, 50, 1, 0, 3, 2, 1000, 7, 9]
+    inp.top_p[:] = [0.0, -1.0, np.nan, 1.0, 1.5, 1e-7, 0.999999, 0.5, 0.9, 0.3, 0.95, 0.0, 1.0, 0.7, np.nan, 0.8]
+    inp.temperature[:] = [1.0, 0.0, -1.0, np.nan, np.inf, 0.5, 2.0, 1e-3, 1e3, 1.0, 0.7, 1.0, 0.9, 1.1, 1.0, 1.0]
+    inp.penalty[:] = [1.2, 0.0, -1.0, np.nan, 1.0, 1.2, 1.2, 2.0, 0.5, 1.2, 1.2, 1.2, 1.2, 1.2, 1.2, 1.2]
+    ref = oracle.sample(inp)
+    gi, gf = run_gpu(inp)
+    compare(inp, ref, gi, gf, "edge params")
+
+
+def test_q_edge_values():
+    inp = make_random(6, 2048, seed=5)
+    inp.q[0, :] = 0.0
+    inp.q[1, ::2] = np.inf
+    inp.q[2, :] = 1.0
+    inp.q[3, 100:200] = np.nan
+    inp.q[4, :] = 1e-30
+    ref = oracle.sample(inp)
+    gi, gf = run_gpu(inp)
+    compare(inp, ref, gi, gf, "q edges")
+
+
+def test_zero_rows_is_noop():
+    import torch
+    import decode_token_sampling_gb300 as kps
+    dev = "cuda:0"
+    z = torch.empty(0, 100, device=dev)
+    idx, f = kps.sample(z, torch.empty(0, dtype=torch.int32, device=dev), torch.empty(0, device=dev),
+                        torch.empty(0, device=dev), torch.empty(0, 100, device=dev))
+    torch.cuda.synchronize()
+    assert idx.numel() == 0 and f is None
+
+
+def test_status_word_clean_after_runs():
+    import torch
+    import decode_token_sampling_gb300 as kps
+    inp = make_random(4, 5000, seed=3)
+    ws = kps.new_workspace(inp.B, inp.V)
+    run_gpu(inp, workspace=ws)
+    assert kps.last_device_status(ws) == 0
+
+
+def test_side_stream_and_repeat_determinism():
+    import torch
+    inp = make_workload("small_mixed")
+    s = torch.cuda.Stream()
+    a = run_gpu(inp, stream=s)
+    b = run_gpu(inp)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
