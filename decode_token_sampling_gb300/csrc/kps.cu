@@ -729,16 +729,22 @@ static int device_sm_count() {
 
 static int round_up8(int64_t x) { return static_cast<int>((x + 7) / 8 * 8); }
 
+// Kernel attributes are per device: set them once for each device that launches.
 template <bool kBF16>
 static cudaError_t prepare_kernel() {
-  static std::once_flag once;
-  static cudaError_t err = cudaSuccess;
-  std::call_once(once, [] {
-    const int optin = device_smem_optin();
-    err = cudaFuncSetAttribute(kps_sample_kernel<kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
-    if (err == cudaSuccess)
-      err = cudaFuncSetAttribute(kps_sample_kernel<kBF16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  });
+  static std::mutex mu;
+  static bool done[64] = {};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[dev]) return cudaSuccess;
+  const int optin = device_smem_optin();
+  err = cudaFuncSetAttribute(kps_sample_kernel<kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+  if (err == cudaSuccess)
+    err = cudaFuncSetAttribute(kps_sample_kernel<kBF16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (err == cudaSuccess) done[dev] = true;
   return err;
 }
 
@@ -928,3 +934,4 @@ kps_status kps_last_device_status(void* workspace, cudaStream_t stream, int* out
 }
 
 }  // extern "C"
+
