@@ -935,3 +935,52 @@ kps_status kps_last_device_status(void* workspace, cudaStream_t stream, int* out
 
 }  // extern "C"
 
+// ------------------------------------------------------------------------------------------
+// No-allocation entry point: the scratch lives in a fixed device array.
+// ------------------------------------------------------------------------------------------
+namespace kps {
+constexpr size_t kNoallocScratchBytes = 4096;
+constexpr int kMaxDevices = 64;
+// File-scope scratch for kps_sample_noalloc.  In host code this name is only a
+// stand-in for the symbol: its device address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+// Device address of g_noalloc_scratch on the current device, looked up once per
+// device with that device current.  Returns nullptr on failure.
+static void* noalloc_scratch_address() {
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return nullptr;
+    }
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+}  // namespace kps
+
+extern "C" kps_status kps_sample_noalloc(const void* logits, kps_dtype dt, int64_t B, int64_t V,
+                                         const int32_t* top_k, const float* top_p, const float* temperature,
+                                         const int32_t* seen_indptr, const int32_t* seen_ids,
+                                         const float* penalty, const float* q, float eps, int need_logits,
+                                         int64_t* out_idx, float* out_filtered, cudaStream_t stream) {
+  const size_t need = kps_workspace_size(B, V, dt);
+  if (need == 0) return KPS_ERR_INVALID_ARG;
+  if (need > kps::kNoallocScratchBytes) return KPS_ERR_UNSUPPORTED;
+  if (B == 0) return KPS_OK;
+  void* scratch = kps::noalloc_scratch_address();
+  if (!scratch) return KPS_ERR_CUDA;
+  // the shared array keeps the previous call's status word: clear it on this stream first
+  if (cudaMemsetAsync(scratch, 0, need, stream) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return KPS_ERR_CUDA;
+  }
+  return kps_sample(logits, dt, B, V, top_k, top_p, temperature, seen_indptr, seen_ids, penalty, q, eps,
+                    need_logits, out_idx, out_filtered, scratch, kps::kNoallocScratchBytes, stream);
+}

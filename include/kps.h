@@ -113,6 +113,36 @@ kps_status kps_sample(const void* logits, kps_dtype dt, int64_t B, int64_t V,
  * stream, stores KPS_OK or the first device-side error code in *out. */
 kps_status kps_last_device_status(void* workspace, cudaStream_t stream, int* out);
 
+/*
+ * kps_sample_noalloc — kps_sample for callers that cannot allocate device
+ * memory.  Some hosts of this library cannot call cudaMalloc: an allocator
+ * that owns all device memory and forbids outside allocations, a real-time
+ * path where allocation latency or failure is not acceptable, or code that
+ * runs under a memory budget it does not control.  This entry point needs no
+ * workspace: its scratch (the device status word) lives in a fixed array
+ * inside the library, 4096 bytes, held on every GPU that loads the library
+ * until the process exits.  It allocates nothing and calls no allocating
+ * routine; the caller still passes inputs and outputs as for kps_sample.
+ * (The method's pages have no counterpart to this entry point.)
+ *
+ *   - Arguments, results and math are exactly those of kps_sample.
+ *   - Calls whose workspace would exceed the 4096-byte scratch are rejected
+ *     with KPS_ERR_UNSUPPORTED before anything is launched.
+ *   - The first call on each device looks up the scratch array's device
+ *     address with that device current (and sets kernel attributes); make
+ *     that first call before capturing the stream into a CUDA graph.
+ *   - Every call on a device shares the one scratch array, which keeps the
+ *     last call's contents; each call clears it on its stream first.  Calls
+ *     that overlap on the GPU (different streams, no ordering between them)
+ *     race on it.  A device-side timeout is recorded there but cannot be read
+ *     back through this entry point.
+ */
+kps_status kps_sample_noalloc(const void* logits, kps_dtype dt, int64_t B, int64_t V,
+                              const int32_t* top_k, const float* top_p, const float* temperature,
+                              const int32_t* seen_indptr, const int32_t* seen_ids,
+                              const float* penalty, const float* q, float eps, int need_logits,
+                              int64_t* out_idx, float* out_filtered, cudaStream_t stream);
+
 /* Static description of a status code. */
 const char* kps_status_string(kps_status s);
 
