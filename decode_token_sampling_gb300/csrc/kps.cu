@@ -1,29 +1,48 @@
 // kps.cu — GB300 (sm_103a) kernels and C ABI for the decode-step sampler.
 //
-// One thread-block cluster owns one row of the [B, V] logits matrix.  The row
-// is split into CS contiguous chunks, one per CTA; each chunk is staged into
-// shared memory with a TMA bulk copy (cp.async.bulk + mbarrier) and stays
-// there for the whole row, so logits are read from HBM exactly once.  All
-// selection steps then run on shared memory, and the CTAs combine their
-// partial results through distributed shared memory (DSMEM) and cluster
-// barriers:
+// A persistent grid of thread-block clusters walks the rows of the [B, V]
+// logits matrix; a cluster of CS CTAs owns one row at a time, CTA r holding
+// the contiguous chunk [r*nc, (r+1)*nc) in shared memory.  Each chunk is
+// staged with a TMA bulk copy (cp.async.bulk + mbarrier), so logits are read
+// from HBM once; CTAs combine partial results through distributed shared
+// memory (DSMEM) and cluster barriers.  Per row:
 //
-//   load  -> penalty (scatter over the seen ids, once per distinct id)
-//         -> temperature (x / T, IEEE) and the row maximum
-//         -> top-k: exact radix select of the k-th element in the order
-//            (value desc, index asc) — 4 passes of 8-bit digits over
-//            order-preserving uint32 keys, count histograms
-//         -> top-p: the same radix select weighted by softmax mass, held
-//            in 2^-40 fixed point so the sums are exact and order-free
-//         -> exponential race: argmax of e / (q + eps) over the kept set
-//         -> filtered logits written back in vocabulary order.
+//   load -> penalty (scatter over the seen ids, once per distinct id)
+//        -> raw pass: NaN -> -inf, -0 -> +0, row maximum and the maximum of
+//           every 128-element group.  Division by a positive temperature is
+//           monotone, so maxima (and any order bound) can be taken before it.
+//   top-k rows (1 < k <= min(V, 1024)):
+//        -> t0 = (a lower bound of) the k-th largest group maximum divided by
+//           T: k groups have a maximum >= it, so the row's k-th value is >= t0.
+//        -> candidate pass: only elements that can reach t0 are divided by T;
+//           those >= t0 are kept in a per-CTA list and counted in 2048 linear
+//           bins of (M - y).  The chunk is then free: the TMA load of the
+//           CTA's next row starts here and overlaps the rest of this row.
+//        -> the bin holding the k-th element is found from the cluster-wide
+//           histogram; its few elements are gathered to every CTA and ranked
+//           exactly, giving the k-th element (value desc, index asc).
+//        -> top-p inside the k survivors: the same bin search weighted by
+//           softmax mass in 2^-40 fixed point, then an exact prefix over the
+//           boundary bin's elements.
+//        -> race over the kept candidates (q gathered at their indices).
+//   top-p-only rows: the chunk is divided by T in place; a mass histogram over
+//        linear bins of (M - x), then a finer one inside the boundary bin,
+//        locates the boundary, resolved exactly as above; the race and the
+//        filtered-logit write are one fused pass.
+//   Any overflow of the small candidate structures falls back to an exact
+//   radix select over the whole resident row.
+//
+// Softmax mass is held in 2^-40 fixed point (uint64), so every sum is exact
+// and independent of summation order; weights are expf of the difference
+// x - max carried exactly (TwoSum).
 //
 // The method follows the Ascend "torch_npu.npu_top_k_top_p_sample" page
 // (topK valid range, topP full-sort rule, Sample formulas), MiniMind
 // "Chapter 10: inference generation" (§10.4 temperature, §10.5 top-k, §10.6
 // top-p, §10.7 repetition penalty) and the C++ post-processing blog
-// (penalty over the set of seen ids, softmax).  Selection is by radix
-// histograms rather than the sorts and quickselects on those pages.
+// (penalty over the set of seen ids, softmax).  Selection is by bounds,
+// histograms and small exact rankings instead of the sorts and quickselects
+// on those pages.
 //
 // Nothing here waits without a bound: the TMA wait gives up after ~2 s of
 // clock cycles, records KPS_ERR_TIMEOUT in the status word and carries on
@@ -46,17 +65,34 @@ namespace kps {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kBins = 256;          // 8-bit radix digits
-constexpr int kSuper = 16;          // super-bins of 16 bins each
+constexpr int kMaxCS = 16;          // widest cluster
+constexpr int kBins = 256;          // 8-bit radix digits (fallback radix select)
+constexpr int kSuper = 16;          // super-bins of 16 bins each (fallback radix select)
 constexpr int kTopKMax = 1024;      // top-k is active for 1 <= k <= min(V, 1024)
+constexpr int kCapLoc = 1024;       // candidates one CTA may hold
+constexpr int kGallCap = 2048;      // group maxima one row may have for the top-k bound
+constexpr int kLinBins = 2048;      // linear bins of the first histogram
+constexpr int kFineBins = 1024;     // linear bins of the refinement histogram (top-p-only rows)
+constexpr int kSmall = 64;          // boundary-bin elements resolved by exact ranking
+constexpr int kMaxChunk = 65536;    // largest per-CTA chunk the layout supports
 constexpr float kFixScale = 1099511627776.0f;  // 2^40: fixed-point unit of softmax mass
 constexpr long long kSpinCycles = 4000000000LL;  // bounded wait (~2 s)
-constexpr int kSmemCap2PerSM = 110 * 1024;  // per-CTA budget for two CTAs per SM
+constexpr int kSmemCap2PerSM = 112 * 1024;  // per-CTA budget for two CTAs per SM
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kStatusTimeout = KPS_ERR_TIMEOUT;
+constexpr uint32_t kKeyNegInf = 0x007FFFFFu;  // key of -inf; key 0 marks padding
 
-// Cluster exchange slots (u64 each) in shared memory.
-enum Slot { kSlotMax = 0, kSlotRace = 1, kSlotTie = 2, kNumSlots = 4 };
+// Shared-memory exchange slots (u64).  Arrays of kMaxCS are filled by every CTA
+// of the cluster (push), so each CTA reduces them locally after the barrier.
+enum Slot {
+  kSlotMax = 0,                       // [kMaxCS] row maximum pushes
+  kSlotRace = kSlotMax + kMaxCS,      // [kMaxCS] race winner pushes
+  kSlotFlag = kSlotRace + kMaxCS,     // [kMaxCS] per-CTA flags
+  kSlotV0 = kSlotFlag + kMaxCS,       // [kMaxCS] first-of-order pushes
+  kSlotTie = kSlotV0 + kMaxCS,        // split tie (fallback radix select)
+  kSlotSmallCnt,                      // size of this CTA's boundary list
+  kNumSlots
+};
 
 struct Params {
   const void* logits;
@@ -74,14 +110,14 @@ struct Params {
   float* out_filtered;
   int* status;
   int nc;       // elements per CTA (multiple of 8)
-  int use_tma;  // every row starts on a 16-byte boundary
+  int use_tma;  // every row of logits, q and out starts on a 16-byte boundary
 };
 
 // ------------------------------------------------------------------------------------------
 // Shared-memory layout (identical on host and device).
 // ------------------------------------------------------------------------------------------
 struct Layout {
-  size_t xs, raw, bitmap, hist, sup, red, slots, mbar, misc, total;
+  size_t xs, raw, cand_key, cand_idx, hist, fine, sup, small, gmax, red, slots, mbar, misc, total;
 };
 
 __host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
@@ -89,15 +125,19 @@ __host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~size_t(
 __host__ __device__ inline Layout make_layout(int nc, bool bf16) {
   Layout L;
   size_t off = 0;
-  L.xs = off;     off += align16(size_t(nc) * 4);
-  L.raw = off;    off += bf16 ? align16(size_t(nc) * 2) : 0;
-  L.bitmap = off; off += align16(size_t((nc + 31) / 32) * 4);
-  L.hist = off;   off += 2 * kBins * 8;
-  L.sup = off;    off += 2 * kSuper * 8;
-  L.red = off;    off += 40 * 8;
-  L.slots = off;  off += kNumSlots * 8;
-  L.mbar = off;   off += 16;
-  L.misc = off;   off += 16 * 8;
+  L.xs = off;       off += align16(size_t(nc) * 4);
+  L.raw = off;      off += bf16 ? align16(size_t(nc) * 2) : 0;
+  L.cand_key = off; off += size_t(kCapLoc) * 4;  // also the penalty bitmap (nc/8 bytes)
+  L.cand_idx = off; off += size_t(kCapLoc) * 4;
+  L.hist = off;     off += size_t(kLinBins) * 8;  // also the gathered group maxima
+  L.fine = off;     off += size_t(kFineBins) * 8;
+  L.sup = off;      off += size_t(kLinBins / 32 + kFineBins / 32) * 8;
+  L.small = off;    off += size_t(2 * kSmall) * 8;  // own boundary list, then the gathered one
+  L.gmax = off;     off += align16(size_t((nc + 127) / 128) * 4);
+  L.red = off;      off += 40 * 8;
+  L.slots = off;    off += size_t(kNumSlots) * 8;
+  L.mbar = off;     off += 16;
+  L.misc = off;     off += 16 * 8;
   L.total = off;
   return L;
 }
@@ -120,6 +160,10 @@ __device__ __forceinline__ float kfloat(uint32_t k) {
 __device__ __forceinline__ bool kept_by(uint32_t key, int32_t idx, uint32_t tk, int32_t ti) {
   return key > tk || (key == tk && idx <= ti);
 }
+// u64 form of an (key, index) pair whose unsigned order is the order (value desc, index asc)
+__device__ __forceinline__ unsigned long long order_word(uint32_t key, int32_t idx) {
+  return (static_cast<unsigned long long>(key) << 32) | static_cast<uint32_t>(~idx);
+}
 
 // Softmax weight exp(x - M) in fp32.  The difference x - M is carried exactly
 // as hi + lo (Knuth's TwoSum) and the exponential is corrected to first order,
@@ -136,6 +180,43 @@ __device__ __forceinline__ float softmax_weight(float x, float M) {
 }
 __device__ __forceinline__ unsigned long long fixed_mass(float w) {
   return __float2ull_rn(w * kFixScale);
+}
+
+// Linear bin of y in [lo, M]: min(nb - 1, floor((M - y) * s)); monotone
+// non-increasing in y (bin 0 holds the largest values).
+__device__ __forceinline__ int lin_bin_scaled(float y, float M, float s, int nb) {
+  if (y == M) return 0;
+  const float d = __fsub_rn(M, y);
+  const float f = __fmul_rn(d, s);
+  if (!(f < static_cast<float>(nb))) return nb - 1;
+  return static_cast<int>(f);
+}
+// First histogram of top-p-only rows: bins of width 1/32 in d = M - x over
+// [0, 64); returns kLinBins for d >= 64 (zero fixed-point mass).
+__device__ __forceinline__ int lin_bin_mass(float x, float M) {
+  if (x == M) return 0;
+  const float d = __fsub_rn(M, x);
+  if (!(d < 64.0f)) return kLinBins;
+  return static_cast<int>(d * 32.0f);
+}
+// Refinement inside first-level bin b: kFineBins bins over d in [b/32, (b+1)/32).
+__device__ __forceinline__ int fine_bin_mass(float x, float M, int b) {
+  const float d = (x == M) ? 0.0f : __fsub_rn(M, x);
+  const float f = __fmul_rn(__fsub_rn(d, static_cast<float>(b) * 0.03125f), 32.0f * kFineBins);
+  if (!(f > 0.0f)) return 0;
+  if (!(f < static_cast<float>(kFineBins))) return kFineBins - 1;
+  return static_cast<int>(f);
+}
+
+// A raw value below which x / T cannot reach t0 = fl(g / T) (T finite > 0):
+// any x < g - 4 * T * ulp(t0) has x / T at least 3.5 ulp below t0.  Returns
+// -inf when t0 is not a normal number with room (then every element is tested).
+__device__ __forceinline__ float raw_lower_bound(float g, float t0, float T) {
+  const float a = fabsf(t0);
+  if (!(a >= 1e-30f) || !(a <= 1e30f) || isinf(g)) return -INFINITY;
+  const float up = __uint_as_float(__float_as_uint(a) + 1u) - a;  // spacing above |t0|
+  const double gap = 4.0 * static_cast<double>(T) * static_cast<double>(up);
+  return __double2float_rd(static_cast<double>(g) - gap);
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -189,16 +270,18 @@ __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
   }
   return v;
 }
-__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
-#pragma unroll
-  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-  return v;
-}
-// Inclusive prefix sum across the warp.
 __device__ __forceinline__ unsigned long long warp_incl_scan_u64(unsigned long long v, int lane) {
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     unsigned long long w = __shfl_up_sync(kFull, v, o);
+    if (lane >= o) v += w;
+  }
+  return v;
+}
+__device__ __forceinline__ uint32_t warp_incl_scan_u32(uint32_t v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    uint32_t w = __shfl_up_sync(kFull, v, o);
     if (lane >= o) v += w;
   }
   return v;
@@ -221,95 +304,130 @@ __device__ unsigned long long block_max_u64(unsigned long long v, unsigned long 
   return v;
 }
 
-// Cluster-wide max of a u64 through one exchange slot; every thread gets it.
-__device__ unsigned long long cluster_max_u64(cg::cluster_group& cl, unsigned long long local,
-                                              unsigned long long* slot, unsigned long long* bcast) {
+// Block-wide exclusive scan of u32 values; *total gets the sum.
+__device__ uint32_t block_excl_scan_u32(uint32_t v, uint32_t* total, unsigned long long* red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int CS = static_cast<int>(cl.num_blocks());
-  if (threadIdx.x == 0) *slot = local;
-  cl.sync();
+  const uint32_t x = warp_incl_scan_u32(v, lane);
+  if (lane == 31) red[warp] = x;
+  __syncthreads();
   if (warp == 0) {
-    unsigned long long v = 0;
-    for (int r = lane; r < CS; r += 32) {
-      unsigned long long w = *cl.map_shared_rank(slot, r);
-      v = w > v ? w : v;
-    }
-    v = warp_max_u64(v);
-    if (lane == 0) *bcast = v;
+    const uint32_t s = lane < kWarps ? static_cast<uint32_t>(red[lane]) : 0u;
+    const uint32_t t = warp_incl_scan_u32(s, lane);
+    if (lane < kWarps) red[lane] = t - s;
+    if (lane == kWarps - 1) red[32] = t;
   }
   __syncthreads();
-  return *bcast;
+  const uint32_t res = static_cast<uint32_t>(red[warp]) + x - v;
+  *total = static_cast<uint32_t>(red[32]);
+  __syncthreads();
+  return res;
+}
+
+// Sum over the cluster of the value at the same shared-memory address in
+// every CTA (loads issued together).
+template <typename T>
+__device__ __forceinline__ T remote_sum(cg::cluster_group& cl, T* p, int CS) {
+  T s = T(0);
+  for (int r = 0; r < CS; r += 4) {
+    T v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = r + u < CS ? *cl.map_shared_rank(p, r + u) : T(0);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) s += v[u];
+  }
+  return s;
+}
+
+// Pushes a u64 into slot array `arr` (index = own rank) of every CTA of the cluster.
+__device__ __forceinline__ void push_all(cg::cluster_group& cl, unsigned long long* arr, int rank, int CS,
+                                         unsigned long long v) {
+  for (int r = 0; r < CS; ++r) *cl.map_shared_rank(arr + rank, r) = v;
+}
+__device__ __forceinline__ unsigned long long max_of(const unsigned long long* arr, int CS) {
+  unsigned long long m = 0;
+  for (int r = 0; r < CS; ++r) m = arr[r] > m ? arr[r] : m;
+  return m;
 }
 
 // ------------------------------------------------------------------------------------------
 // Per-CTA context for one row
 // ------------------------------------------------------------------------------------------
 struct Ctx {
-  float* xs;            // transformed values of this CTA's chunk
+  float* xs;            // this CTA's chunk (raw, then transformed where a path needs it)
   int32_t c0;           // row index of xs[0]
   int n;                // elements in this chunk
   int n4;               // float4 groups covering the chunk (tail padded with key 0)
   float M;              // row maximum (transformed)
-  unsigned long long* hist;  // [2][kBins]
-  unsigned long long* sup;   // [2][kSuper]
+  uint32_t* cand_key;   // candidate list of this CTA (transformed keys)
+  int32_t* cand_idx;
+  unsigned long long* hist;  // kLinBins u64 (fallback radix uses two 256-bin halves)
+  unsigned long long* fine;  // kFineBins u64
+  unsigned long long* sup;   // kLinBins/32 + kFineBins/32 u64 (fallback radix uses two 16-entry halves)
+  unsigned long long* small; // [kSmall] own boundary list, [kSmall] gathered list
+  uint32_t* gmax;            // this CTA's group maxima (raw keys)
   unsigned long long* red;
   unsigned long long* slots;
   unsigned long long* misc;
 };
 
-// Result of a radix select: the last kept element's key and index.
+// Result of a selection: the last kept element's key and index.
 struct Thresh {
   uint32_t key;
   int32_t idx;
 };
 
-// Block-wide exclusive scan of small counts; returns the exclusive prefix, *total gets the sum.
-__device__ uint32_t block_excl_scan_u32(uint32_t v, uint32_t* total, unsigned long long* red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    uint32_t w = __shfl_up_sync(kFull, x, o);
-    if (lane >= o) x += w;
-  }
-  if (lane == 31) red[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    uint32_t s = lane < kWarps ? static_cast<uint32_t>(red[lane]) : 0u;
-    uint32_t t = s;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      uint32_t w = __shfl_up_sync(kFull, t, o);
-      if (lane >= o) t += w;
-    }
-    if (lane < kWarps) red[lane] = t - s;  // exclusive prefix of warp totals
-    if (lane == kWarps - 1) red[32] = t;
-  }
-  __syncthreads();
-  uint32_t res = static_cast<uint32_t>(red[warp]) + x - v;
-  *total = static_cast<uint32_t>(red[32]);
-  __syncthreads();
-  return res;
-}
-
-// Finds, in index order, the j-th (1-based) element of this CTA's chunk with
-// key == tkey that is kept by (rk, ri).  Returns its row index, or -1.
-__device__ int32_t local_nth_tie(const Ctx& c, uint32_t tkey, uint32_t rk, int32_t ri, uint32_t j) {
-  int32_t* found = reinterpret_cast<int32_t*>(c.misc + 8);
-  if (threadIdx.x == 0) *found = -1;
-  __syncthreads();
-  for (int base = 0; base < c.n4; base += kThreads) {
-    const int g = base + threadIdx.x;
-    uint32_t cnt = 0;
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (g < c.n4) {
-      v = reinterpret_cast<const float4*>(c.xs)[g];
+// Element sources for the fallback radix select.  for_each calls
+// f(valid, key, index, value) with the whole warp converged.
+struct SrcData {  // the CTA's resident chunk (transformed values)
+  const float* xs;
+  int n4;
+  int32_t c0;
+  template <class F>
+  __device__ __forceinline__ void for_each(F&& f) const {
+    for (int base = 0; base < n4; base += kThreads) {
+      const int g = base + threadIdx.x;
+      const bool in = g < n4;
+      const float4 v = in ? reinterpret_cast<const float4*>(xs)[g] : make_float4(0.f, 0.f, 0.f, 0.f);
       const float vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const uint32_t key = fkey(vv[e]);
-        const int32_t gi = c.c0 + 4 * g + e;
-        cnt += (key == tkey && key != 0 && kept_by(key, gi, rk, ri)) ? 1u : 0u;
+        f(in && key != 0u, key, c0 + 4 * g + e, vv[e]);
+      }
+    }
+  }
+};
+struct SrcCand {  // this CTA's candidate list (unordered)
+  const uint32_t* key;
+  const int32_t* idx;
+  int n;
+  template <class F>
+  __device__ __forceinline__ void for_each(F&& f) const {
+    for (int base = 0; base < n; base += kThreads) {
+      const int i = base + threadIdx.x;
+      const bool in = i < n;
+      const uint32_t k = in ? key[i] : 0u;
+      f(in && k != 0u, k, in ? idx[i] : 0, kfloat(k));
+    }
+  }
+};
+
+// j-th (1-based) smallest index among this CTA's elements with key == tkey kept by (rk, ri).
+__device__ int32_t nth_tie(const SrcData& s, const Ctx& c, uint32_t tkey, uint32_t rk, int32_t ri, uint32_t j) {
+  int32_t* found = reinterpret_cast<int32_t*>(c.misc + 8);
+  if (threadIdx.x == 0) *found = -1;
+  __syncthreads();
+  for (int base = 0; base < s.n4; base += kThreads) {
+    const int g = base + threadIdx.x;
+    uint32_t cnt = 0;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (g < s.n4) {
+      v = reinterpret_cast<const float4*>(s.xs)[g];
+      const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t key = fkey(vv[e]);
+        cnt += (key == tkey && key != 0 && kept_by(key, s.c0 + 4 * g + e, rk, ri)) ? 1u : 0u;
       }
     }
     uint32_t total;
@@ -320,35 +438,51 @@ __device__ int32_t local_nth_tie(const Ctx& c, uint32_t tkey, uint32_t rk, int32
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const uint32_t key = fkey(vv[e]);
-        const int32_t gi = c.c0 + 4 * g + e;
-        if (key == tkey && key != 0 && kept_by(key, gi, rk, ri)) {
+        if (key == tkey && key != 0 && kept_by(key, s.c0 + 4 * g + e, rk, ri)) {
           ++seen;
-          if (seen == j) *found = gi;
+          if (seen == j) *found = s.c0 + 4 * g + e;
         }
       }
     }
     __syncthreads();
     const int32_t f = *found;
     if (f >= 0) return f;
-    if (total >= j) return -1;  // inconsistent (cannot happen for valid data)
+    if (total >= j) return -1;
     j -= total;
   }
   return -1;
 }
+// Same over the (unordered) candidate list: the tie whose index has exactly j-1
+// smaller tie indices.
+__device__ int32_t nth_tie(const SrcCand& s, const Ctx& c, uint32_t tkey, uint32_t rk, int32_t ri, uint32_t j) {
+  int32_t* found = reinterpret_cast<int32_t*>(c.misc + 8);
+  if (threadIdx.x == 0) *found = -1;
+  __syncthreads();
+  for (int i = threadIdx.x; i < s.n; i += kThreads) {
+    if (s.key[i] != tkey || !kept_by(s.key[i], s.idx[i], rk, ri)) continue;
+    uint32_t smaller = 0;
+    for (int m = 0; m < s.n; ++m)
+      smaller += (s.key[m] == tkey && s.idx[m] < s.idx[i] && kept_by(s.key[m], s.idx[m], rk, ri)) ? 1u : 0u;
+    if (smaller + 1 == j) *found = s.idx[i];
+  }
+  __syncthreads();
+  return *found;
+}
 
-// Exact radix select over the cluster's row, restricted to the elements kept by
-// (rk, ri).  kMass = false: find the k-th element of the order (target = k).
-// kMass = true: find the shortest prefix of the order whose softmax mass
-// reaches p * (mass of the restricted set).  Returns the threshold of the
-// selected prefix.  Every CTA of the cluster computes the same answer.
-template <bool kMass>
-__device__ Thresh radix_select(cg::cluster_group& cl, Ctx& c, unsigned long long target_k, float p,
-                               uint32_t rk, int32_t ri) {
+// Exact distributed radix select over the cluster's elements from `src`,
+// restricted to those kept by (rk, ri).  kMass = false: the target is a count
+// (find the target-th element of the order).  kMass = true: the target is a
+// fixed-point mass (find the shortest prefix whose mass reaches it); with
+// p_mode the target is ceil(p * total mass of the restricted set).  Returns
+// the threshold of the selected prefix.  Every CTA computes the same answer.
+// Used when the fast paths' small structures overflow.
+template <class Src, bool kMass>
+__device__ Thresh radix_select(cg::cluster_group& cl, Ctx& c, const Src& src, unsigned long long target,
+                               bool p_mode, float p, uint32_t rk, int32_t ri) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int CS = static_cast<int>(cl.num_blocks());
-  const float4* x4 = reinterpret_cast<const float4*>(c.xs);
   uint32_t prefix = 0, pmask = 0;
-  unsigned long long tau = target_k;
+  unsigned long long tau = target;
   unsigned long long tie_weight = 0;
   bool ok = true;
   int cur = 0;
@@ -358,20 +492,19 @@ __device__ Thresh radix_select(cg::cluster_group& cl, Ctx& c, unsigned long long
     unsigned long long* s = c.sup + cur * kSuper;
     for (int i = threadIdx.x; i < kBins; i += kThreads) h[i] = 0ull;
     __syncthreads();
-    for (int g = threadIdx.x; g < c.n4; g += kThreads) {
-      const float4 v = x4[g];
-      const float vv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const uint32_t key = fkey(vv[e]);
-        const int32_t gi = c.c0 + 4 * g + e;
-        if (key != 0 && (key & pmask) == prefix && kept_by(key, gi, rk, ri)) {
-          unsigned long long w = 1ull;
-          if (kMass) w = fixed_mass(softmax_weight(vv[e], c.M));
-          if (w) atomicAdd(&h[(key >> shift) & 0xFF], w);
+    src.for_each([&](bool valid, uint32_t key, int32_t idx, float x) {
+      const bool take = valid && (key & pmask) == prefix && kept_by(key, idx, rk, ri);
+      const int bin = static_cast<int>((key >> shift) & 0xFFu);
+      if (kMass) {
+        if (take) {
+          const unsigned long long w = fixed_mass(softmax_weight(x, c.M));
+          if (w) atomicAdd(&h[bin], w);
         }
+      } else {
+        const unsigned peers = __match_any_sync(kFull, take ? bin : -1);
+        if (take && lane == __ffs(peers) - 1) atomicAdd(&h[bin], static_cast<unsigned long long>(__popc(peers)));
       }
-    }
+    });
     __syncthreads();
     if (threadIdx.x < kBins) {
       unsigned long long v = h[threadIdx.x];
@@ -382,19 +515,19 @@ __device__ Thresh radix_select(cg::cluster_group& cl, Ctx& c, unsigned long long
     cl.sync();
     if (warp == 0) {
       // super-bins, largest keys first: lane l covers super-bin 15 - l
-      unsigned long long sv = 0;
-      if (lane < kSuper)
-        for (int r = 0; r < CS; ++r) sv += *cl.map_shared_rank(s + (kSuper - 1 - lane), r);
-      if (kMass && d == 0) {
-        const unsigned long long total = warp_sum_u64(sv);
-        double t = ceil(static_cast<double>(p) * static_cast<double>(total));
+      const unsigned long long sv = lane < kSuper ? remote_sum(cl, s + (kSuper - 1 - (lane & 15)), CS) : 0ull;
+      if (p_mode && d == 0) {
+        unsigned long long total = sv;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) total += __shfl_xor_sync(kFull, total, o);
+        const double t = ceil(static_cast<double>(p) * static_cast<double>(total));
         unsigned long long tt = static_cast<unsigned long long>(t);
         if (tt < 1ull) tt = 1ull;
         if (tt > total) tt = total;
         tau = tt;
       }
       const unsigned long long inc = warp_incl_scan_u64(sv, lane);
-      unsigned m = __ballot_sync(kFull, lane < kSuper && inc >= tau);
+      const unsigned m = __ballot_sync(kFull, lane < kSuper && inc >= tau);
       unsigned long long bin_w = 0, new_tau = tau;
       int beta = 0;
       bool good = (m != 0u) && tau > 0;
@@ -402,9 +535,7 @@ __device__ Thresh radix_select(cg::cluster_group& cl, Ctx& c, unsigned long long
         const int L = __ffs(m) - 1;
         const unsigned long long above = L > 0 ? __shfl_sync(kFull, inc, L - 1) : 0ull;
         const int sigma = kSuper - 1 - L;
-        unsigned long long bv = 0;
-        if (lane < 16)
-          for (int r = 0; r < CS; ++r) bv += *cl.map_shared_rank(h + sigma * 16 + (15 - lane), r);
+        const unsigned long long bv = lane < 16 ? remote_sum(cl, h + sigma * 16 + (15 - (lane & 15)), CS) : 0ull;
         const unsigned long long inc2 = warp_incl_scan_u64(bv, lane);
         const unsigned m2 = __ballot_sync(kFull, lane < 16 && above + inc2 >= tau);
         if (m2 == 0u) {
@@ -422,7 +553,6 @@ __device__ Thresh radix_select(cg::cluster_group& cl, Ctx& c, unsigned long long
         c.misc[1] = new_tau;
         c.misc[2] = bin_w;
         c.misc[3] = good ? 1ull : 0ull;
-        c.misc[4] = tau;
       }
     }
     __syncthreads();
@@ -439,7 +569,6 @@ __device__ Thresh radix_select(cg::cluster_group& cl, Ctx& c, unsigned long long
   if (!ok) return Thresh{rk, ri};  // degenerate input: keep the whole restricted set
 
   const uint32_t key = prefix;
-  // weight of one element equal to the threshold key
   const unsigned long long w1 = kMass ? fixed_mass(softmax_weight(kfloat(key), c.M)) : 1ull;
   if (w1 == 0ull) return Thresh{key, key == rk ? ri : INT_MAX};
   const unsigned long long ties = tie_weight / w1;
@@ -447,17 +576,17 @@ __device__ Thresh radix_select(cg::cluster_group& cl, Ctx& c, unsigned long long
   if (need >= ties) return Thresh{key, key == rk ? ri : INT_MAX};
 
   // Split inside the ties: the need-th tie in index order.  CTAs own contiguous
-  // index ranges in rank order, so find the owner from the per-CTA tie counts
-  // (the last pass's local histograms, still intact), then search it.
+  // index ranges in rank order; the owner comes from the per-CTA tie counts
+  // (the last pass's local histograms, still intact).
   const int last = cur ^ 1;
   const int beta_last = static_cast<int>(key & 0xFFu);
-  int owner = -1;
-  unsigned long long jloc = 0;
   if (warp == 0) {
     unsigned long long t = 0;
     if (lane < CS) t = *cl.map_shared_rank(c.hist + last * kBins + beta_last, lane) / w1;
     const unsigned long long inc = warp_incl_scan_u64(t, lane);
     const unsigned m = __ballot_sync(kFull, lane < CS && inc >= need);
+    int owner = -1;
+    unsigned long long jloc = 0;
     if (m) {
       const int L = __ffs(m) - 1;
       const unsigned long long before = L > 0 ? __shfl_sync(kFull, inc, L - 1) : 0ull;
@@ -470,16 +599,14 @@ __device__ Thresh radix_select(cg::cluster_group& cl, Ctx& c, unsigned long long
     }
   }
   __syncthreads();
-  owner = static_cast<int>(static_cast<long long>(c.misc[5]));
-  jloc = c.misc[6];
+  const int owner = static_cast<int>(static_cast<long long>(c.misc[5]));
+  const unsigned long long jloc = c.misc[6];
   __syncthreads();
-  const int rank = static_cast<int>(cl.block_rank());
-  if (rank == owner) {
-    const int32_t f = local_nth_tie(c, key, rk, ri, static_cast<uint32_t>(jloc));
-    if (threadIdx.x == 0) {
+  if (static_cast<int>(cl.block_rank()) == owner) {
+    const int32_t f = nth_tie(src, c, key, rk, ri, static_cast<uint32_t>(jloc));
+    if (threadIdx.x == 0)
       for (int r = 0; r < CS; ++r)
         *cl.map_shared_rank(c.slots + kSlotTie, r) = static_cast<unsigned long long>(static_cast<uint32_t>(f));
-    }
   }
   cl.sync();
   int32_t ti = static_cast<int32_t>(static_cast<uint32_t>(c.slots[kSlotTie]));
@@ -487,8 +614,201 @@ __device__ Thresh radix_select(cg::cluster_group& cl, Ctx& c, unsigned long long
   return Thresh{key, ti};
 }
 
+// k-th largest (k >= 1) of n keys in shared memory, rounded down to a multiple
+// of 2^(32 - 8*passes) (so it is <= the exact k-th largest); block-local.
+// Uses the first 256 words of hist as a count histogram.
+__device__ uint32_t local_kth_largest(Ctx& c, const uint32_t* keys, int n, uint32_t k, int passes) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t* h = reinterpret_cast<uint32_t*>(c.hist);
+  uint32_t prefix = 0, pmask = 0;
+  for (int d = 0; d < passes; ++d) {
+    const int shift = 24 - 8 * d;
+    for (int i = threadIdx.x; i < kBins; i += kThreads) h[i] = 0u;
+    __syncthreads();
+    for (int base = 0; base < n; base += kThreads) {
+      const int i = base + threadIdx.x;
+      const uint32_t key = i < n ? keys[i] : 0u;
+      const bool take = i < n && (key & pmask) == prefix;
+      const int bin = static_cast<int>((key >> shift) & 0xFFu);
+      const unsigned peers = __match_any_sync(kFull, take ? bin : -1);
+      if (take && lane == __ffs(peers) - 1) atomicAdd(&h[bin], static_cast<uint32_t>(__popc(peers)));
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane l owns bins 255 - 8l ... 248 - 8l (largest first)
+      uint32_t b[8];
+      uint32_t sum = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        b[e] = h[255 - 8 * lane - e];
+        sum += b[e];
+      }
+      const uint32_t inc = warp_incl_scan_u32(sum, lane);
+      const unsigned m = __ballot_sync(kFull, inc >= k);
+      if (m) {
+        const int L = __ffs(m) - 1;
+        if (lane == L) {
+          uint32_t acc = inc - sum;
+          int beta = 255 - 8 * lane;
+          uint32_t newk = k - acc;
+          for (int e = 0; e < 8; ++e) {
+            if (acc + b[e] >= k) {
+              beta = 255 - 8 * lane - e;
+              newk = k - acc;
+              break;
+            }
+            acc += b[e];
+          }
+          c.misc[0] = static_cast<unsigned long long>(beta);
+          c.misc[1] = newk;
+        }
+      } else if (lane == 0) {
+        c.misc[0] = 0ull;  // cannot happen for k <= n
+        c.misc[1] = 1ull;
+      }
+    }
+    __syncthreads();
+    prefix |= static_cast<uint32_t>(c.misc[0]) << shift;
+    pmask |= 0xFFu << shift;
+    k = static_cast<uint32_t>(c.misc[1]);
+    __syncthreads();
+  }
+  return prefix;
+}
+
+// After cl.sync: scans the cluster-wide histogram (nb bins in `h`, super sums
+// of 32 bins in `sup`, both per CTA) in increasing bin order for the first bin
+// where the cumulative weight reaches tau (p_mode: tau = ceil(p * total)).
+struct Boundary {
+  int beta;                 // -1 when no bin reaches tau
+  unsigned long long above; // weight of the bins before beta
+  unsigned long long binw;  // weight of bin beta
+  unsigned long long tau;   // target used
+};
+__device__ Boundary find_boundary(cg::cluster_group& cl, Ctx& c, unsigned long long* h,
+                                  unsigned long long* sup, int nb, unsigned long long tau, bool p_mode,
+                                  float p) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int CS = static_cast<int>(cl.num_blocks());
+  const int nsup = nb / 32;
+  if (warp == 0) {
+    const int i0 = 2 * lane, i1 = 2 * lane + 1;
+    const unsigned long long s0 = i0 < nsup ? remote_sum(cl, sup + (i0 < nsup ? i0 : 0), CS) : 0ull;
+    const unsigned long long s1 = i1 < nsup ? remote_sum(cl, sup + (i1 < nsup ? i1 : 0), CS) : 0ull;
+    const unsigned long long inc = warp_incl_scan_u64(s0 + s1, lane);
+    if (p_mode) {
+      const unsigned long long total = __shfl_sync(kFull, inc, 31);
+      const double t = ceil(static_cast<double>(p) * static_cast<double>(total));
+      unsigned long long tt = static_cast<unsigned long long>(t);
+      if (tt < 1ull) tt = 1ull;
+      if (tt > total) tt = total;
+      tau = tt;
+    }
+    const unsigned m = __ballot_sync(kFull, inc >= tau && tau > 0);
+    int beta = -1;
+    unsigned long long above = 0, binw = 0;
+    if (m) {
+      const int Ls = __ffs(m) - 1;
+      const unsigned long long before = Ls > 0 ? __shfl_sync(kFull, inc, Ls - 1) : 0ull;
+      const unsigned long long s0L = __shfl_sync(kFull, s0, Ls);
+      const int sigma = (before + s0L >= tau) ? 2 * Ls : 2 * Ls + 1;
+      const unsigned long long abv = (sigma == 2 * Ls) ? before : before + s0L;
+      const unsigned long long bv = remote_sum(cl, h + sigma * 32 + lane, CS);
+      const unsigned long long inc2 = warp_incl_scan_u64(bv, lane);
+      const unsigned m2 = __ballot_sync(kFull, abv + inc2 >= tau);
+      if (m2) {
+        const int L2 = __ffs(m2) - 1;
+        above = abv + (L2 > 0 ? __shfl_sync(kFull, inc2, L2 - 1) : 0ull);
+        binw = __shfl_sync(kFull, bv, L2);
+        beta = sigma * 32 + L2;
+      }
+    }
+    if (lane == 0) {
+      c.misc[0] = static_cast<unsigned long long>(static_cast<long long>(beta));
+      c.misc[1] = above;
+      c.misc[2] = binw;
+      c.misc[3] = tau;
+    }
+  }
+  __syncthreads();
+  Boundary b;
+  b.beta = static_cast<int>(static_cast<long long>(c.misc[0]));
+  b.above = c.misc[1];
+  b.binw = c.misc[2];
+  b.tau = c.misc[3];
+  __syncthreads();
+  return b;
+}
+
+// Super sums of 32 bins (nb bins in h) into sup; block-wide, before cl.sync.
+__device__ __forceinline__ void super_sums(const unsigned long long* h, unsigned long long* sup, int nb) {
+  for (int t = threadIdx.x; t < nb / 4; t += kThreads) {
+    unsigned long long v = h[4 * t] + h[4 * t + 1] + h[4 * t + 2] + h[4 * t + 3];
+    v += __shfl_xor_sync(kFull, v, 1);
+    v += __shfl_xor_sync(kFull, v, 2);
+    v += __shfl_xor_sync(kFull, v, 4);
+    if ((t & 7) == 0) sup[t >> 3] = v;
+  }
+}
+
+// After cl.sync: gathers every CTA's boundary list (order words, count in
+// kSlotSmallCnt) into the second half of c.small and finds, among them, the
+// element whose exclusive prefix weight in the order satisfies
+// excl < need <= excl + w (count mode: w = 1; mass mode: w = fixed mass).
+// Returns false (uniformly) if the lists do not fit.
+template <bool kMass>
+__device__ bool resolve_small(cg::cluster_group& cl, Ctx& c, unsigned long long need, Thresh* out) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int CS = static_cast<int>(cl.num_blocks());
+  unsigned long long* all = c.small + kSmall;
+  uint32_t* meta = reinterpret_cast<uint32_t*>(c.misc + 12);  // [0] total, [1] found
+  uint32_t* offs = reinterpret_cast<uint32_t*>(c.red);       // [kMaxCS] list offsets
+  if (warp == 0) {
+    const uint32_t cnt = lane < CS ? static_cast<uint32_t>(*cl.map_shared_rank(c.slots + kSlotSmallCnt, lane)) : 0u;
+    const uint32_t inc = warp_incl_scan_u32(cnt, lane);
+    const uint32_t tot = __shfl_sync(kFull, inc, 31);
+    const bool fits = __all_sync(kFull, cnt <= static_cast<uint32_t>(kSmall)) && tot <= static_cast<uint32_t>(kSmall);
+    if (lane < CS) offs[lane] = inc - cnt;
+    if (lane == 0) {
+      meta[0] = fits ? tot : 0xFFFFFFFFu;
+      meta[1] = 0u;
+    }
+  }
+  __syncthreads();
+  const uint32_t total = meta[0];
+  if (total == 0xFFFFFFFFu) {
+    __syncthreads();
+    return false;
+  }
+  for (uint32_t t = threadIdx.x; t < total; t += kThreads) {
+    int r = 0;
+    while (r + 1 < CS && offs[r + 1] <= t) ++r;
+    all[t] = *cl.map_shared_rank(c.small + (t - offs[r]), r);
+  }
+  __syncthreads();
+  for (uint32_t i = threadIdx.x; i < total; i += kThreads) {
+    const unsigned long long wi = all[i];
+    unsigned long long excl = 0, self = 1;
+    if (kMass) self = fixed_mass(softmax_weight(kfloat(static_cast<uint32_t>(wi >> 32)), c.M));
+    for (uint32_t j = 0; j < total; ++j) {
+      const unsigned long long wj = all[j];
+      if (wj > wi)
+        excl += kMass ? fixed_mass(softmax_weight(kfloat(static_cast<uint32_t>(wj >> 32)), c.M)) : 1ull;
+    }
+    if (excl < need && need <= excl + self) {
+      out->key = static_cast<uint32_t>(wi >> 32);
+      out->idx = static_cast<int32_t>(~static_cast<uint32_t>(wi));
+      meta[1] = 1u;
+    }
+  }
+  __syncthreads();
+  const bool ok = meta[1] != 0u;
+  __syncthreads();
+  return ok;
+}
+
 // ------------------------------------------------------------------------------------------
-// The kernel: one cluster per row.
+// The kernel: a persistent grid of clusters, one row per cluster at a time.
 // ------------------------------------------------------------------------------------------
 template <bool kBF16>
 __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P) {
@@ -496,213 +816,597 @@ __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P)
   extern __shared__ __align__(16) unsigned char smem[];
   const Layout L = make_layout(P.nc, kBF16);
   float* xs = reinterpret_cast<float*>(smem + L.xs);
-  uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem + L.bitmap);
+  uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem + L.cand_key);
   unsigned long long* mbar = reinterpret_cast<unsigned long long*>(smem + L.mbar);
+  // block-shared scalars live in the dynamic layout (misc[14], misc[15])
+  uint32_t& sh_cnt = *reinterpret_cast<uint32_t*>(smem + L.misc + 14 * 8);
+  Thresh& sh_thresh = *reinterpret_cast<Thresh*>(smem + L.misc + 15 * 8);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
   const int CS = static_cast<int>(cl.num_blocks());
   const int rank = static_cast<int>(cl.block_rank());
-  const int64_t row = blockIdx.x / CS;
   const int64_t V = P.V;
   const int32_t c0 = rank * P.nc;
   int n = static_cast<int>(V - c0);
   n = n < 0 ? 0 : (n > P.nc ? P.nc : n);
   const int n4 = (n + 3) >> 2;
+  const size_t esize = kBF16 ? 2 : 4;
+  const uint32_t bytes = static_cast<uint32_t>(n * esize);
+  const bool tma = P.use_tma && bytes > 0;
+  const int64_t cid = blockIdx.x / CS;
+  const int64_t ncl = gridDim.x / CS;
 
   Ctx c;
   c.xs = xs;
   c.c0 = c0;
   c.n = n;
   c.n4 = n4;
+  c.cand_key = reinterpret_cast<uint32_t*>(smem + L.cand_key);
+  c.cand_idx = reinterpret_cast<int32_t*>(smem + L.cand_idx);
   c.hist = reinterpret_cast<unsigned long long*>(smem + L.hist);
+  c.fine = reinterpret_cast<unsigned long long*>(smem + L.fine);
   c.sup = reinterpret_cast<unsigned long long*>(smem + L.sup);
+  c.small = reinterpret_cast<unsigned long long*>(smem + L.small);
+  c.gmax = reinterpret_cast<uint32_t*>(smem + L.gmax);
   c.red = reinterpret_cast<unsigned long long*>(smem + L.red);
   c.slots = reinterpret_cast<unsigned long long*>(smem + L.slots);
   c.misc = reinterpret_cast<unsigned long long*>(smem + L.misc);
 
-  // ---- stage this CTA's chunk into shared memory --------------------------------------
-  const size_t esize = kBF16 ? 2 : 4;
   void* stage = kBF16 ? static_cast<void*>(smem + L.raw) : static_cast<void*>(xs);
-  const unsigned char* gsrc = static_cast<const unsigned char*>(P.logits) + (row * V + c0) * esize;
-  const uint32_t bytes = static_cast<uint32_t>(n * esize);
-  const bool tma = P.use_tma && bytes > 0;
-  if (threadIdx.x == 0) mbar_init(mbar, 1);
-  __syncthreads();
-  if (tma && threadIdx.x == 0) {
-    mbar_expect_tx(mbar, bytes);
-    constexpr uint32_t kPiece = 16384;
-    for (uint32_t off = 0; off < bytes; off += kPiece) {
-      const uint32_t len = bytes - off < kPiece ? bytes - off : kPiece;
-      bulk_g2s(static_cast<unsigned char*>(stage) + off, gsrc + off, len, mbar);
-    }
-  }
-
-  // row parameters (uniform across the cluster)
-  const int32_t k = P.top_k[row];
-  const float p = P.top_p[row];
-  const float T = P.temperature[row];
-  const bool greedyT = !(T > 0.0f) || isinf(T);
-  const bool pen_on = P.seen_indptr && P.seen_ids && P.penalty && (P.penalty[row] > 0.0f);
-  const float pen = pen_on ? P.penalty[row] : 1.0f;
-  const bool topk_on = k >= 1 && static_cast<int64_t>(k) <= (V < kTopKMax ? V : kTopKMax);
-  const bool p_nan = isnan(p);
-  const bool single = greedyT || (!p_nan && p <= 0.0f) || (topk_on && k == 1);
-  const bool topp_on = !single && !p_nan && p > 0.0f && p < 1.0f;
-
-  if (pen_on)
-    for (int w = threadIdx.x; w < (n + 31) / 32; w += kThreads) bitmap[w] = 0u;
-
-  if (!tma) {
-    for (int i = threadIdx.x; i < n; i += kThreads) {
-      if (kBF16) {
-        const __nv_bfloat16 h = reinterpret_cast<const __nv_bfloat16*>(gsrc)[i];
-        xs[i] = __bfloat162float(h);
-      } else {
-        xs[i] = reinterpret_cast<const float*>(gsrc)[i];
+  auto gsrc_of = [&](int64_t row) {
+    return static_cast<const unsigned char*>(P.logits) + (row * V + c0) * esize;
+  };
+  auto issue_load = [&](int64_t row) {
+    if (tma && threadIdx.x == 0) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_expect_tx(mbar, bytes);
+      constexpr uint32_t kPiece = 16384;
+      const unsigned char* src = gsrc_of(row);
+      for (uint32_t off = 0; off < bytes; off += kPiece) {
+        const uint32_t len = bytes - off < kPiece ? bytes - off : kPiece;
+        bulk_g2s(static_cast<unsigned char*>(stage) + off, src + off, len, mbar);
       }
     }
-  }
-  bool timed_out = false;
-  if (tma) {
-    if (!mbar_wait_bounded(mbar, 0)) {
-      timed_out = true;
-      if (threadIdx.x == 0) atomicMax(P.status, kStatusTimeout);
-    }
-  }
-  if (kBF16 && tma) {
-    const __nv_bfloat16* raw = reinterpret_cast<const __nv_bfloat16*>(smem + L.raw);
-    for (int i = threadIdx.x; i < n; i += kThreads) xs[i] = __bfloat162float(raw[i]);
-  }
-  __syncthreads();
+  };
 
-  // ---- repetition penalty: scatter over the seen ids, once per distinct id --------------
-  if (pen_on) {
-    const int32_t b0 = P.seen_indptr[row], b1 = P.seen_indptr[row + 1];
-    for (int32_t j = b0 + threadIdx.x; j < b1; j += kThreads) {
-      const int32_t id = P.seen_ids[j];
-      const int32_t li = id - c0;
-      if (id >= 0 && static_cast<int64_t>(id) < V && li >= 0 && li < n) {
-        const uint32_t bit = 1u << (li & 31);
-        const uint32_t old = atomicOr(&bitmap[li >> 5], bit);
-        if (!(old & bit)) {
-          const float s = xs[li];
-          xs[li] = (s > 0.0f) ? __fdiv_rn(s, pen) : __fmul_rn(s, pen);
-        }
+  if (threadIdx.x == 0) mbar_init(mbar, 1);
+  __syncthreads();
+  if (cid < P.B) issue_load(cid);
+  bool timed_out = false;
+  uint32_t parity = 0;
+
+  for (int64_t row = cid; row < P.B; row += ncl, parity ^= 1u) {
+    const int64_t next = row + ncl;
+    bool next_issued = false;
+
+    // ---- row parameters (uniform across the cluster) ---------------------------------
+    const int32_t k = P.top_k[row];
+    const float p = P.top_p[row];
+    const float T = P.temperature[row];
+    const bool greedyT = !(T > 0.0f) || isinf(T);
+    const bool pen_on = P.seen_indptr && P.seen_ids && P.penalty && (P.penalty[row] > 0.0f);
+    const float pen = pen_on ? P.penalty[row] : 1.0f;
+    const bool topk_on = k >= 1 && static_cast<int64_t>(k) <= (V < kTopKMax ? V : kTopKMax);
+    const bool p_nan = isnan(p);
+    const bool single = greedyT || (!p_nan && p <= 0.0f) || (topk_on && k == 1);
+    const bool topp_on = !single && !p_nan && p > 0.0f && p < 1.0f;
+
+    // prefetch up to four seen ids per thread while the chunk is in flight
+    int32_t pid[4];
+    int32_t b0 = 0, b1 = 0;
+    if (pen_on) {
+      b0 = P.seen_indptr[row];
+      b1 = P.seen_indptr[row + 1];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int32_t j = b0 + threadIdx.x + u * kThreads;
+        pid[u] = j < b1 ? P.seen_ids[j] : -1;
+      }
+      for (int w = threadIdx.x; w < (n + 31) / 32; w += kThreads) bitmap[w] = 0u;
+    }
+
+    // ---- wait for the chunk --------------------------------------------------------
+    if (!tma) {
+      const unsigned char* src = gsrc_of(row);
+      for (int i = threadIdx.x; i < n; i += kThreads) {
+        if (kBF16) xs[i] = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(src)[i]);
+        else xs[i] = reinterpret_cast<const float*>(src)[i];
+      }
+    } else {
+      if (!mbar_wait_bounded(mbar, parity)) {
+        timed_out = true;
+        if (threadIdx.x == 0) atomicMax(P.status, kStatusTimeout);
+      }
+      if (kBF16) {
+        const __nv_bfloat16* raw = reinterpret_cast<const __nv_bfloat16*>(smem + L.raw);
+        for (int i = threadIdx.x; i < n; i += kThreads) xs[i] = __bfloat162float(raw[i]);
       }
     }
     __syncthreads();
-  }
 
-  // ---- temperature, NaN -> -inf, padding, row maximum -----------------------------------
-  unsigned long long best = 0;  // (key << 32) | ~index: max gives max key, then lowest index
-  {
-    float4* x4 = reinterpret_cast<float4*>(xs);
-    for (int g = threadIdx.x; g < n4; g += kThreads) {
-      float4 v = x4[g];
-      float vv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i = 4 * g + e;
-        float x = vv[e];
-        if (i >= n) {
-          x = __uint_as_float(0xFFFFFFFFu);  // padding: key 0
-        } else {
-          if (isnan(x)) x = -INFINITY;
-          if (!greedyT) x = __fdiv_rn(x, T);
-          x = __fadd_rn(x, 0.0f);  // -0 -> +0: equal values share one key
-          const unsigned long long cand =
-              (static_cast<unsigned long long>(fkey(x)) << 32) | static_cast<uint32_t>(~(c0 + i));
-          best = cand > best ? cand : best;
+    // ---- repetition penalty: scatter over the seen ids, once per distinct id -----------
+    if (pen_on) {
+      auto apply = [&](int32_t id) {
+        const int32_t li = id - c0;
+        if (id >= 0 && static_cast<int64_t>(id) < V && li >= 0 && li < n) {
+          const uint32_t bit = 1u << (li & 31);
+          const uint32_t old = atomicOr(&bitmap[li >> 5], bit);
+          if (!(old & bit)) {
+            const float s = xs[li];
+            xs[li] = (s > 0.0f) ? __fdiv_rn(s, pen) : __fmul_rn(s, pen);
+          }
         }
-        vv[e] = x;
-      }
-      x4[g] = make_float4(vv[0], vv[1], vv[2], vv[3]);
-    }
-  }
-  best = block_max_u64(best, c.red);
-  const unsigned long long rowbest = cluster_max_u64(cl, best, c.slots + kSlotMax, c.misc + 10);
-  const uint32_t mkey = static_cast<uint32_t>(rowbest >> 32);
-  const int32_t v0 = static_cast<int32_t>(~static_cast<uint32_t>(rowbest));
-  c.M = kfloat(mkey);
-
-  // ---- selection: top-k then top-p, as one threshold in the order -----------------------
-  Thresh th{0u, -1};  // keeps every real element (padding has key 0)
-  if (single) {
-    th = Thresh{mkey, v0};
-  } else {
-    if (topk_on) th = radix_select<false>(cl, c, static_cast<unsigned long long>(k), 0.0f, th.key, th.idx);
-    if (topp_on) th = radix_select<true>(cl, c, 0ull, p, th.key, th.idx);
-  }
-
-  // ---- exponential race over the kept set ----------------------------------------------
-  int32_t chosen = v0;
-  if (!single) {
-    const float* qrow = P.q + row * V;
-    const bool q_vec = P.use_tma != 0;  // same 16-byte alignment condition as the logits rows
-    unsigned long long rb = 0;
-    const float4* x4 = reinterpret_cast<const float4*>(xs);
-    for (int g = threadIdx.x; g < n4; g += kThreads) {
-      const float4 v = x4[g];
-      const float vv[4] = {v.x, v.y, v.z, v.w};
-      bool kp[4];
-      int nk = 0;
+      };
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        kp[e] = kept_by(fkey(vv[e]), c0 + 4 * g + e, th.key, th.idx);
-        nk += kp[e];
+      for (int u = 0; u < 4; ++u) apply(pid[u]);
+      for (int32_t j = b0 + threadIdx.x + 4 * kThreads; j < b1; j += kThreads) apply(P.seen_ids[j]);
+      __syncthreads();
+    }
+
+    // ---- raw pass: NaN -> -inf, -0 -> +0, padding, group maxima, chunk maximum --------
+    uint32_t tmax = 0;
+    {
+      float4* x4 = reinterpret_cast<float4*>(xs);
+      for (int base = 0; base < n4; base += kThreads) {
+        const int g = base + threadIdx.x;
+        uint32_t gk = 0;
+        if (g < n4) {
+          const float4 v = x4[g];
+          float vv[4] = {v.x, v.y, v.z, v.w};
+          bool changed = false;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float x = vv[e];
+            float y;
+            if (4 * g + e >= n) y = __uint_as_float(0xFFFFFFFFu);  // padding: key 0
+            else y = isnan(x) ? -INFINITY : __fadd_rn(x, 0.0f);
+            changed |= __float_as_uint(y) != __float_as_uint(x);
+            const uint32_t key = fkey(y);
+            gk = key > gk ? key : gk;
+            vv[e] = y;
+          }
+          if (changed) x4[g] = make_float4(vv[0], vv[1], vv[2], vv[3]);
+        }
+        // the warp's 32 float4s are one group of 128 consecutive elements
+        gk = __reduce_max_sync(kFull, gk);
+        if (lane == 0 && base + 32 * warp < n4) c.gmax[(base >> 5) + warp] = gk;
+        tmax = gk > tmax ? gk : tmax;
       }
-      if (!nk) continue;
-      float qq[4];
-      if (nk == 4 && q_vec) {
-        const float4 q4 = __ldcs(reinterpret_cast<const float4*>(qrow + c0) + g);
-        qq[0] = q4.x; qq[1] = q4.y; qq[2] = q4.z; qq[3] = q4.w;
+    }
+    {
+      const unsigned long long m = block_max_u64(tmax, c.red);
+      if (threadIdx.x == 0) push_all(cl, c.slots + kSlotMax, rank, CS, m);
+      cl.sync();
+    }
+    const uint32_t mraw_key = static_cast<uint32_t>(max_of(c.slots + kSlotMax, CS));
+    const float Mraw = kfloat(mraw_key);
+    const float M = greedyT ? Mraw : __fdiv_rn(Mraw, T);  // max of x / T is (max x) / T
+    c.M = M;
+    const uint32_t mkey = fkey(M);
+
+    float* orow = P.need_logits ? P.out_filtered + row * V + c0 : nullptr;
+    bool neg_inf_written = false;
+    auto write_neg_inf = [&]() {
+      if (P.use_tma && (n & 3) == 0) {
+        const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        for (int g = threadIdx.x; g < n4; g += kThreads) __stcs(reinterpret_cast<float4*>(orow) + g, ninf);
       } else {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) qq[e] = kp[e] ? __ldcs(qrow + c0 + 4 * g + e) : 0.0f;
+        for (int i = threadIdx.x; i < n; i += kThreads) orow[i] = -INFINITY;
       }
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        if (!kp[e]) continue;
-        const float w = softmax_weight(vv[e], c.M);
-        const float r = __fdiv_rn(w, __fadd_rn(qq[e], P.eps));
-        if (isnan(r)) continue;
-        const unsigned long long cand = (static_cast<unsigned long long>(fkey(r)) << 32) |
-                                        static_cast<uint32_t>(~(c0 + 4 * g + e));
-        rb = cand > rb ? cand : rb;
-      }
-    }
-    rb = block_max_u64(rb, c.red);
-    rb = cluster_max_u64(cl, rb, c.slots + kSlotRace, c.misc + 11);
-    if (rb != 0ull) chosen = static_cast<int32_t>(~static_cast<uint32_t>(rb));
-  }
+      neg_inf_written = true;
+    };
 
-  // ---- filtered logits in vocabulary order -------------------------------------------
-  if (P.need_logits && n > 0) {
-    float* orow = P.out_filtered + row * V + c0;
-    const float4* x4 = reinterpret_cast<const float4*>(xs);
-    if (P.use_tma && (n & 3) == 0) {
+    Thresh th{0u, -1};  // keeps every real element (padding has key 0)
+    int32_t chosen = -1;
+    bool cand_mode = false;  // kept set and values live in the candidate lists
+    int ncand = 0;
+    bool transformed = greedyT;  // xs holds transformed values
+
+    auto transform_in_place = [&]() {
+      if (transformed) return;
+      float4* x4 = reinterpret_cast<float4*>(xs);
       for (int g = threadIdx.x; g < n4; g += kThreads) {
-        const float4 v = x4[g];
-        float4 o;
-        o.x = kept_by(fkey(v.x), c0 + 4 * g + 0, th.key, th.idx) ? v.x : -INFINITY;
-        o.y = kept_by(fkey(v.y), c0 + 4 * g + 1, th.key, th.idx) ? v.y : -INFINITY;
-        o.z = kept_by(fkey(v.z), c0 + 4 * g + 2, th.key, th.idx) ? v.z : -INFINITY;
-        o.w = kept_by(fkey(v.w), c0 + 4 * g + 3, th.key, th.idx) ? v.w : -INFINITY;
-        __stcs(reinterpret_cast<float4*>(orow) + g, o);
+        float4 v = x4[g];
+        if (4 * g + 0 < n) v.x = __fdiv_rn(v.x, T);
+        if (4 * g + 1 < n) v.y = __fdiv_rn(v.y, T);
+        if (4 * g + 2 < n) v.z = __fdiv_rn(v.z, T);
+        if (4 * g + 3 < n) v.w = __fdiv_rn(v.w, T);
+        x4[g] = v;
       }
-    } else {
+      __syncthreads();
+      transformed = true;
+    };
+    // First element of the order among this CTA's elements whose transformed value
+    // equals M, pushed and reduced over the cluster.
+    auto first_of_order = [&]() -> int32_t {
+      const float lo = transformed ? M : raw_lower_bound(Mraw, M, T);
+      unsigned long long b = 0;
       for (int i = threadIdx.x; i < n; i += kThreads) {
         const float x = xs[i];
-        orow[i] = kept_by(fkey(x), c0 + i, th.key, th.idx) ? x : -INFINITY;
+        if (!(x >= lo)) continue;
+        const float y = transformed ? x : __fdiv_rn(x, T);
+        if (fkey(y) == mkey) {
+          const unsigned long long w = order_word(mkey, c0 + i);
+          b = w > b ? w : b;
+        }
+      }
+      b = block_max_u64(b, c.red);
+      if (threadIdx.x == 0) push_all(cl, c.slots + kSlotV0, rank, CS, b);
+      cl.sync();
+      return static_cast<int32_t>(~static_cast<uint32_t>(max_of(c.slots + kSlotV0, CS)));
+    };
+
+    if (single) {
+      // ---- one element kept: the first of the order -----------------------------
+      chosen = first_of_order();
+      th = Thresh{mkey, chosen};
+    } else if (topk_on) {
+      // ---- top-k: lower bound from the group maxima ------------------------------
+      const int ng_full = (P.nc + 127) / 128;
+      int G = 0;
+      for (int r = 0; r < CS; ++r) {
+        int nr = static_cast<int>(V - static_cast<int64_t>(r) * P.nc);
+        nr = nr < 0 ? 0 : (nr > P.nc ? P.nc : nr);
+        G += (((nr + 3) >> 2) + 31) >> 5;
+      }
+      bool fast = G >= k && G <= kGallCap;
+      if (fast) {
+        uint32_t* gall = reinterpret_cast<uint32_t*>(c.hist) + kBins;  // after the 256 count words
+        for (int i = threadIdx.x; i < G; i += kThreads) {
+          const int r = i / ng_full, j = i - r * ng_full;
+          gall[i] = *cl.map_shared_rank(c.gmax + j, r);
+        }
+        __syncthreads();
+        uint32_t gkey = local_kth_largest(c, gall, G, static_cast<uint32_t>(k), 3);
+        if (gkey < kKeyNegInf) gkey = kKeyNegInf;
+        const float g = kfloat(gkey);  // <= the k-th largest raw group maximum
+        const float t0 = __fdiv_rn(g, T);
+        const uint32_t t0key = fkey(t0);
+        const float lo = raw_lower_bound(g, t0, T);
+        const float span = __fsub_rn(M, t0);
+        const float s = (span > 0.0f && span < INFINITY) ? __fdiv_rn(static_cast<float>(kLinBins), span) : 0.0f;
+        // candidate pass: count histogram over linear bins of (M - y)
+        __syncthreads();  // gall (inside hist) is dead from here
+        for (int i = threadIdx.x; i < kLinBins; i += kThreads) c.hist[i] = 0ull;
+        if (threadIdx.x == 0) sh_cnt = 0u;
+        __syncthreads();
+        const float4* x4 = reinterpret_cast<const float4*>(xs);
+        for (int base = 0; base < n4; base += kThreads) {
+          const int gi = base + threadIdx.x;
+          uint32_t ck[4] = {0u, 0u, 0u, 0u};
+          int cnt = 0;
+          if (gi < n4) {
+            const float4 v = x4[gi];
+            const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              if (vv[e] >= lo && fkey(vv[e]) != 0u) {
+                const float y = __fdiv_rn(vv[e], T);
+                const uint32_t ky = fkey(y);
+                if (ky >= t0key) {
+                  ck[e] = ky;
+                  ++cnt;
+                  const int b = s > 0.0f ? lin_bin_scaled(y, M, s, kLinBins) : 0;
+                  atomicAdd(&c.hist[b], 1ull);
+                }
+              }
+            }
+          }
+          const uint32_t incl = warp_incl_scan_u32(static_cast<uint32_t>(cnt), lane);
+          const uint32_t wtot = __shfl_sync(kFull, incl, 31);
+          if (wtot) {
+            uint32_t wb = 0;
+            if (lane == 31) wb = atomicAdd(&sh_cnt, wtot);
+            wb = __shfl_sync(kFull, wb, 31);
+            uint32_t pos = wb + incl - cnt;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              if (ck[e]) {
+                if (pos < static_cast<uint32_t>(kCapLoc)) {
+                  c.cand_key[pos] = ck[e];
+                  c.cand_idx[pos] = c0 + 4 * gi + e;
+                }
+                ++pos;
+              }
+            }
+          }
+        }
+        // the filtered output is -inf outside the kept set: stream it now, the kept
+        // values are scattered over it at the end of the row
+        if (orow) write_neg_inf();
+        __syncthreads();
+        ncand = static_cast<int>(sh_cnt);
+        super_sums(c.hist, c.sup, kLinBins);
+        if (threadIdx.x == 0) push_all(cl, c.slots + kSlotFlag, rank, CS, ncand <= kCapLoc ? 1ull : 0ull);
+        cl.sync();
+        bool lists_ok = true;
+        for (int r = 0; r < CS; ++r) lists_ok = lists_ok && c.slots[kSlotFlag + r] != 0ull;
+        const Boundary bk = find_boundary(cl, c, c.hist, c.sup, kLinBins, static_cast<unsigned long long>(k), false, 0.0f);
+        fast = lists_ok && bk.beta >= 0 && bk.binw <= static_cast<unsigned long long>(kSmall);
+        if (fast) {
+          // the k-th element lies in bin beta: rank that bin's elements exactly
+          if (threadIdx.x == 0) sh_cnt = 0u;
+          __syncthreads();
+          for (int i = threadIdx.x; i < ncand; i += kThreads) {
+            const uint32_t key = c.cand_key[i];
+            const int b = s > 0.0f ? lin_bin_scaled(kfloat(key), M, s, kLinBins) : 0;
+            if (b == bk.beta) {
+              const uint32_t pos = atomicAdd(&sh_cnt, 1u);
+              if (pos < static_cast<uint32_t>(kSmall)) c.small[pos] = order_word(key, c.cand_idx[i]);
+            }
+          }
+          __syncthreads();
+          if (threadIdx.x == 0) c.slots[kSlotSmallCnt] = sh_cnt;
+          cl.sync();
+          Thresh tk{0u, -1};
+          if (threadIdx.x == 0) sh_thresh = Thresh{0u, -1};
+          __syncthreads();
+          fast = resolve_small<false>(cl, c, static_cast<unsigned long long>(k) - bk.above, &sh_thresh);
+          tk = sh_thresh;
+          __syncthreads();
+          if (fast) {
+            // the chunk is no longer needed: start the next row's load now
+            __syncthreads();
+            if (next < P.B) {
+              issue_load(next);
+              next_issued = true;
+            }
+            cand_mode = true;
+            th = tk;
+            if (topp_on) {
+              // mass histogram of the k survivors over linear bins of (M - y)
+              const float xk = kfloat(tk.key);
+              const float span2 = __fsub_rn(M, xk);
+              const float s2 =
+                  (span2 > 0.0f && span2 < INFINITY) ? __fdiv_rn(static_cast<float>(kLinBins), span2) : 0.0f;
+              // hist is still read by other CTAs until the next barrier: use `fine` as a
+              // 1024-bin histogram (half resolution)
+              for (int i = threadIdx.x; i < kFineBins; i += kThreads) c.fine[i] = 0ull;
+              __syncthreads();
+              for (int i = threadIdx.x; i < ncand; i += kThreads) {
+                const uint32_t key = c.cand_key[i];
+                if (!kept_by(key, c.cand_idx[i], tk.key, tk.idx)) continue;
+                const float y = kfloat(key);
+                const int b = s2 > 0.0f ? (lin_bin_scaled(y, M, s2, kLinBins) >> 1) : 0;
+                const unsigned long long w = fixed_mass(softmax_weight(y, M));
+                if (w) atomicAdd(&c.fine[b], w);
+              }
+              __syncthreads();
+              super_sums(c.fine, c.sup, kFineBins);
+              cl.sync();
+              const Boundary bp = find_boundary(cl, c, c.fine, c.sup, kFineBins, 0ull, true, p);
+              bool ok2 = bp.beta >= 0;
+              if (ok2) {
+                if (threadIdx.x == 0) sh_cnt = 0u;
+                __syncthreads();
+                for (int i = threadIdx.x; i < ncand; i += kThreads) {
+                  const uint32_t key = c.cand_key[i];
+                  if (!kept_by(key, c.cand_idx[i], tk.key, tk.idx)) continue;
+                  const int b = s2 > 0.0f ? (lin_bin_scaled(kfloat(key), M, s2, kLinBins) >> 1) : 0;
+                  if (b == bp.beta) {
+                    const uint32_t pos = atomicAdd(&sh_cnt, 1u);
+                    if (pos < static_cast<uint32_t>(kSmall)) c.small[pos] = order_word(key, c.cand_idx[i]);
+                  }
+                }
+                __syncthreads();
+                if (threadIdx.x == 0) c.slots[kSlotSmallCnt] = sh_cnt;
+              }
+              cl.sync();
+              if (ok2) {
+                if (threadIdx.x == 0) sh_thresh = tk;
+                __syncthreads();
+                ok2 = resolve_small<true>(cl, c, bp.tau - bp.above, &sh_thresh);
+                th = sh_thresh;
+                __syncthreads();
+              }
+              if (!ok2) {
+                const SrcCand scand{c.cand_key, c.cand_idx, ncand};
+                th = radix_select<SrcCand, true>(cl, c, scand, 0ull, true, p, tk.key, tk.idx);
+              }
+            }
+          }
+        }
+      }
+      if (!cand_mode) {
+        // exact fallback over the whole resident row; the barrier first lets every CTA
+        // finish reading the histograms the fast attempt left in shared memory
+        cl.sync();
+        transform_in_place();
+        const SrcData sdata{xs, n4, c0};
+        const Thresh tk = radix_select<SrcData, false>(cl, c, sdata, static_cast<unsigned long long>(k), false,
+                                                       0.0f, 0u, -1);
+        th = tk;
+        if (topp_on) th = radix_select<SrcData, true>(cl, c, sdata, 0ull, true, p, tk.key, tk.idx);
+      }
+    } else if (topp_on) {
+      // ---- top-p over the whole row ----------------------------------------------
+      transform_in_place();
+      unsigned long long* h = c.hist;
+      for (int i = threadIdx.x; i < kLinBins; i += kThreads) h[i] = 0ull;
+      __syncthreads();
+      const float4* x4 = reinterpret_cast<const float4*>(xs);
+      for (int g = threadIdx.x; g < n4; g += kThreads) {
+        const float4 v = x4[g];
+        const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (fkey(vv[e]) == 0u) continue;
+          const int b = lin_bin_mass(vv[e], M);
+          if (b < kLinBins) {
+            const unsigned long long w = fixed_mass(softmax_weight(vv[e], M));
+            if (w) atomicAdd(&h[b], w);
+          }
+        }
+      }
+      __syncthreads();
+      super_sums(h, c.sup, kLinBins);
+      cl.sync();
+      const Boundary b1 = find_boundary(cl, c, h, c.sup, kLinBins, 0ull, true, p);
+      bool ok = b1.beta >= 0;
+      Boundary b2{-1, 0, 0, 0};
+      if (ok) {
+        // finer histogram inside bin beta (into `fine`; hist is still being read)
+        for (int i = threadIdx.x; i < kFineBins; i += kThreads) c.fine[i] = 0ull;
+        __syncthreads();
+        for (int g = threadIdx.x; g < n4; g += kThreads) {
+          const float4 v = x4[g];
+          const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            if (fkey(vv[e]) == 0u || lin_bin_mass(vv[e], M) != b1.beta) continue;
+            const unsigned long long w = fixed_mass(softmax_weight(vv[e], M));
+            if (w) atomicAdd(&c.fine[fine_bin_mass(vv[e], M, b1.beta)], w);
+          }
+        }
+        __syncthreads();
+        // super sums go to the second half of sup (the first half is still being read)
+        super_sums(c.fine, c.sup + kLinBins / 32, kFineBins);
+      }
+      cl.sync();
+      if (ok) {
+        b2 = find_boundary(cl, c, c.fine, c.sup + kLinBins / 32, kFineBins, b1.tau - b1.above, false, 0.0f);
+        ok = b2.beta >= 0;
+      }
+      if (ok) {
+        if (threadIdx.x == 0) sh_cnt = 0u;
+        __syncthreads();
+        for (int g = threadIdx.x; g < n4; g += kThreads) {
+          const float4 v = x4[g];
+          const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const uint32_t key = fkey(vv[e]);
+            if (key == 0u || lin_bin_mass(vv[e], M) != b1.beta || fine_bin_mass(vv[e], M, b1.beta) != b2.beta) continue;
+            const uint32_t pos = atomicAdd(&sh_cnt, 1u);
+            if (pos < static_cast<uint32_t>(kSmall)) c.small[pos] = order_word(key, c0 + 4 * g + e);
+          }
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) c.slots[kSlotSmallCnt] = sh_cnt;
+      }
+      cl.sync();
+      if (ok) {
+        if (threadIdx.x == 0) sh_thresh = Thresh{0u, -1};
+        __syncthreads();
+        ok = resolve_small<true>(cl, c, b2.tau - b2.above, &sh_thresh);
+        th = sh_thresh;
+        __syncthreads();
+      }
+      if (!ok) {
+        const SrcData sdata{xs, n4, c0};
+        th = radix_select<SrcData, true>(cl, c, sdata, 0ull, true, p, 0u, -1);
+      }
+    } else {
+      transform_in_place();  // top-k and top-p both skipped: every element is kept
+    }
+
+    // ---- exponential race over the kept set, and the filtered-logit write --------------
+    const float* qrow = P.q + row * V;
+    unsigned long long rb = 0;
+    if (single) {
+      // nothing to race
+    } else if (cand_mode) {
+      for (int i = threadIdx.x; i < ncand; i += kThreads) {
+        const uint32_t key = c.cand_key[i];
+        const int32_t idx = c.cand_idx[i];
+        if (!kept_by(key, idx, th.key, th.idx)) continue;
+        const float w = softmax_weight(kfloat(key), M);
+        const float r = __fdiv_rn(w, __fadd_rn(__ldg(qrow + idx), P.eps));
+        if (isnan(r)) continue;
+        const unsigned long long cand = order_word(fkey(r), idx);
+        rb = cand > rb ? cand : rb;
+      }
+    } else {
+      const bool vec = P.use_tma != 0 && (n & 3) == 0;
+      const float4* x4 = reinterpret_cast<const float4*>(xs);
+      for (int g = threadIdx.x; g < n4; g += kThreads) {
+        const float4 v = x4[g];
+        const float vv[4] = {v.x, v.y, v.z, v.w};
+        bool kp[4];
+        int nk = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          kp[e] = kept_by(fkey(vv[e]), c0 + 4 * g + e, th.key, th.idx);
+          nk += kp[e];
+        }
+        if (orow) {
+          if (vec) {
+            __stcs(reinterpret_cast<float4*>(orow) + g,
+                   make_float4(kp[0] ? vv[0] : -INFINITY, kp[1] ? vv[1] : -INFINITY, kp[2] ? vv[2] : -INFINITY,
+                               kp[3] ? vv[3] : -INFINITY));
+          } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (4 * g + e < n) orow[4 * g + e] = kp[e] ? vv[e] : -INFINITY;
+          }
+        }
+        if (!nk) continue;
+        float qq[4];
+        if (nk == 4 && vec) {
+          const float4 q4 = __ldcs(reinterpret_cast<const float4*>(qrow + c0) + g);
+          qq[0] = q4.x; qq[1] = q4.y; qq[2] = q4.z; qq[3] = q4.w;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) qq[e] = kp[e] ? __ldcs(qrow + c0 + 4 * g + e) : 0.0f;
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (!kp[e]) continue;
+          const float w = softmax_weight(vv[e], M);
+          const float r = __fdiv_rn(w, __fadd_rn(qq[e], P.eps));
+          if (isnan(r)) continue;
+          const unsigned long long cand = order_word(fkey(r), c0 + 4 * g + e);
+          rb = cand > rb ? cand : rb;
+        }
       }
     }
-  }
-  if (rank == 0 && threadIdx.x == 0) P.out_idx[row] = chosen;
+    if (!single) {
+      rb = block_max_u64(rb, c.red);
+      if (threadIdx.x == 0) push_all(cl, c.slots + kSlotRace, rank, CS, rb);
+      cl.sync();
+      rb = max_of(c.slots + kSlotRace, CS);
+      if (rb != 0ull) {
+        chosen = static_cast<int32_t>(~static_cast<uint32_t>(rb));
+      } else if (cand_mode) {
+        // every score was NaN: the first element of the order (the best candidate)
+        unsigned long long b = 0;
+        for (int i = threadIdx.x; i < ncand; i += kThreads) {
+          const unsigned long long w = order_word(c.cand_key[i], c.cand_idx[i]);
+          b = w > b ? w : b;
+        }
+        b = block_max_u64(b, c.red);
+        if (threadIdx.x == 0) push_all(cl, c.slots + kSlotV0, rank, CS, b);
+        cl.sync();
+        chosen = static_cast<int32_t>(~static_cast<uint32_t>(max_of(c.slots + kSlotV0, CS)));
+      } else {
+        chosen = first_of_order();
+      }
+    }
 
-  // a CTA that gave up on its copy waits (bounded) for it before leaving
-  if (timed_out) (void)mbar_wait_bounded(mbar, 0);
+    // filtered logits for the paths that did not write them above
+    if (orow && (single || cand_mode)) {
+      if (!neg_inf_written) write_neg_inf();
+      __syncthreads();
+      if (single) {
+        if (threadIdx.x == 0 && th.idx >= c0 && th.idx < c0 + n) orow[th.idx - c0] = M;
+      } else {
+        for (int i = threadIdx.x; i < ncand; i += kThreads)
+          if (kept_by(c.cand_key[i], c.cand_idx[i], th.key, th.idx)) orow[c.cand_idx[i] - c0] = kfloat(c.cand_key[i]);
+      }
+    }
+    if (rank == 0 && threadIdx.x == 0) P.out_idx[row] = chosen;
+
+    // the chunk buffer is free: start the next row's load if it has not started yet
+    __syncthreads();
+    if (!next_issued && next < P.B) issue_load(next);
+  }
+
+  // a CTA that gave up on a copy waits (bounded) for it before leaving
+  if (timed_out) (void)mbar_wait_bounded(mbar, parity);
   // no CTA leaves while another may still read its shared memory
   cl.sync();
 }
+
 
 // ------------------------------------------------------------------------------------------
 // Host side
@@ -711,6 +1415,7 @@ struct LaunchCfg {
   int cs;
   int nc;
   size_t smem;
+  int clusters;  // clusters that can be resident at once (the persistent grid size)
 };
 
 static int device_smem_optin() {
@@ -740,12 +1445,36 @@ static cudaError_t prepare_kernel() {
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(mu);
   if (done[dev]) return cudaSuccess;
-  const int optin = device_smem_optin();
+  cudaFuncAttributes fa;
+  err = cudaFuncGetAttributes(&fa, kps_sample_kernel<kBF16>);
+  if (err != cudaSuccess) return err;
+  const int optin = device_smem_optin() - static_cast<int>(fa.sharedSizeBytes);
   err = cudaFuncSetAttribute(kps_sample_kernel<kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
   if (err == cudaSuccess)
     err = cudaFuncSetAttribute(kps_sample_kernel<kBF16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (err == cudaSuccess) done[dev] = true;
   return err;
+}
+
+template <bool kBF16>
+static int active_clusters(int cs, size_t smem) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cs);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute a[1];
+  a[0].id = cudaLaunchAttributeClusterDimension;
+  a[0].val.clusterDim.x = cs;
+  a[0].val.clusterDim.y = 1;
+  a[0].val.clusterDim.z = 1;
+  cfg.attrs = a;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kps_sample_kernel<kBF16>, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  return n;
 }
 
 template <bool kBF16>
@@ -783,12 +1512,12 @@ static kps_status choose_launch(int64_t B, int64_t V, LaunchCfg* out) {
   for (int cs : sizes) {
     if (cs > 8) break;
     const int nc = round_up8((V + cs - 1) / cs);
-    if (make_layout(nc, kBF16).total <= static_cast<size_t>(kSmemCap2PerSM)) { pick = cs; break; }
+    if (nc <= kMaxChunk && make_layout(nc, kBF16).total <= static_cast<size_t>(kSmemCap2PerSM)) { pick = cs; break; }
   }
   if (pick < 0) {
     for (int cs : sizes) {
       const int nc = round_up8((V + cs - 1) / cs);
-      if (make_layout(nc, kBF16).total <= static_cast<size_t>(optin) &&
+      if (nc <= kMaxChunk && make_layout(nc, kBF16).total <= static_cast<size_t>(optin) &&
           cluster_fits<kBF16>(cs, make_layout(nc, kBF16).total)) { pick = cs; break; }
     }
   }
@@ -802,7 +1531,8 @@ static kps_status choose_launch(int64_t B, int64_t V, LaunchCfg* out) {
   out->cs = pick;
   out->nc = round_up8((V + pick - 1) / pick);
   out->smem = make_layout(out->nc, kBF16).total;
-  if (!cluster_fits<kBF16>(out->cs, out->smem)) return KPS_ERR_UNSUPPORTED;
+  out->clusters = active_clusters<kBF16>(out->cs, out->smem);
+  if (out->clusters <= 0) return KPS_ERR_UNSUPPORTED;
   return KPS_OK;
 }
 
@@ -823,7 +1553,7 @@ int64_t kps_max_vocab(kps_dtype dt) {
   if (optin <= 0) return 0;
   const bool bf = dt == KPS_BF16;
   // largest chunk that fits one CTA, times the widest cluster
-  int lo = 8, hi = 1 << 20;
+  int lo = 8, hi = kps::kMaxChunk;
   while (lo < hi) {
     const int mid = ((lo + hi + 1) / 2) / 8 * 8;
     if (mid <= lo) break;
@@ -902,7 +1632,8 @@ kps_status kps_sample(const void* logits, kps_dtype dt, int64_t B, int64_t V, co
   P.use_tma = aligned ? 1 : 0;
 
   cudaLaunchConfig_t lc = {};
-  lc.gridDim = dim3(static_cast<unsigned>(B * cfg.cs));
+  const int64_t clusters = B < cfg.clusters ? B : cfg.clusters;  // persistent: clusters walk the rows
+  lc.gridDim = dim3(static_cast<unsigned>(clusters * cfg.cs));
   lc.blockDim = dim3(kps::kThreads);
   lc.dynamicSmemBytes = cfg.smem;
   lc.stream = stream;
