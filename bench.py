@@ -216,6 +216,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel", default="auto", choices=["auto", "cluster", "stream"],
+                    help="kernel policy (auto picks per shape; both compute the same results)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -237,6 +239,8 @@ def main():
     dev = torch.device("cuda", local if ws > 1 else 0)
     torch.cuda.set_device(dev)
     kbuild.build()
+    kps.set_kernel_policy({"auto": kps.KERNEL_AUTO, "cluster": kps.KERNEL_CLUSTER,
+                           "stream": kps.KERNEL_STREAM}[args.kernel])
 
     inp = make_workload(args.workload)
     B, V = inp.B, inp.V

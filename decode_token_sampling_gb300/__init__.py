@@ -51,6 +51,10 @@ def load_library() -> ctypes.CDLL:
     lib.kps_last_device_status.argtypes = [P, P, ctypes.POINTER(I32)]
     lib.kps_status_string.restype = ctypes.c_char_p
     lib.kps_status_string.argtypes = [I32]
+    lib.kps_set_kernel_policy.restype = I32
+    lib.kps_set_kernel_policy.argtypes = [I32]
+    lib.kps_get_kernel_policy.restype = I32
+    lib.kps_get_kernel_policy.argtypes = []
     lib.kps_query_launch.restype = I32
     lib.kps_query_launch.argtypes = [I64, I64, I32, ctypes.POINTER(I32), ctypes.POINTER(I64),
                                      ctypes.POINTER(ctypes.c_size_t)]
@@ -94,6 +98,20 @@ def new_workspace(B: int, V: int, dtype: torch.dtype = torch.float32, device="cu
     """A zeroed workspace buffer (uint8) of the size kps_sample needs."""
     n = max(workspace_size(B, V, dtype), 256)
     return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+KERNEL_AUTO, KERNEL_CLUSTER, KERNEL_STREAM = 0, 1, 2
+
+
+def set_kernel_policy(policy: int) -> None:
+    """Process-wide kernel choice: KERNEL_AUTO, KERNEL_CLUSTER or KERNEL_STREAM (see include/kps.h)."""
+    st = load_library().kps_set_kernel_policy(int(policy))
+    if st != 0:
+        raise KpsError(st, "kps_set_kernel_policy")
+
+
+def get_kernel_policy() -> int:
+    return int(load_library().kps_get_kernel_policy())
 
 
 def query_launch(B: int, V: int, dtype: torch.dtype = torch.float32) -> dict:

@@ -71,7 +71,8 @@ constexpr int kSuper = 16;          // super-bins of 16 bins each (fallback radi
 constexpr int kTopKMax = 1024;      // top-k is active for 1 <= k <= min(V, 1024)
 constexpr int kCapLoc = 1024;       // candidates one CTA may hold
 constexpr int kGallCap = 2048;      // group maxima one row may have for the top-k bound
-constexpr int kLinBins = 2048;      // linear bins of the first histogram
+constexpr int kLinBins = 2048;      // linear count bins of the top-k candidate pass
+constexpr int kLinBinsP = 1024;     // linear mass bins (width 1/16 of d = max - x) of top-p-only rows
 constexpr int kFineBins = 1024;     // linear bins of the refinement histogram (top-p-only rows)
 constexpr int kSmall = 64;          // boundary-bin elements resolved by exact ranking
 constexpr int kMaxChunk = 65536;    // largest per-CTA chunk the layout supports
@@ -111,13 +112,59 @@ struct Params {
   int* status;
   int nc;       // elements per CTA (multiple of 8)
   int use_tma;  // every row of logits, q and out starts on a 16-byte boundary
+  int filter;   // rows this launch takes: 0 all, 1 top-k/one-element rows, 2 the others
 };
+
+constexpr int kMaxRowList = 256;  // rows one worker (CTA or cluster) may own in a filtered launch
+
+// True for rows of the one-pass top-k path: top-k active, or a single element kept
+// (greedy temperature, top_p <= 0, or k == 1).  Every kernel and worker agrees on it.
+__device__ __forceinline__ bool row_is_kmode(const Params& P, int64_t row) {
+  const int32_t k = P.top_k[row];
+  const float p = P.top_p[row];
+  const float T = P.temperature[row];
+  const bool greedyT = !(T > 0.0f) || isinf(T);
+  const bool topk_on = k >= 1 && static_cast<int64_t>(k) <= (P.V < 1024 ? P.V : 1024);
+  return topk_on || greedyT || (!isnan(p) && p <= 0.0f);
+}
+
+// Rows worker w of nw owns in a filtered launch: the matching rows whose rank among
+// matching rows is w mod nw, in row order, written to list; returns how many.
+template <int NT>
+__device__ int build_row_list(const Params& P, int64_t w, int64_t nw, int32_t* list, unsigned long long* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  constexpr int NW = NT / 32;
+  int64_t running = 0;
+  int count = 0;
+  for (int64_t base = 0; base < P.B; base += NT) {
+    const int64_t row = base + threadIdx.x;
+    const bool m = row < P.B && (row_is_kmode(P, row) == (P.filter == 1));
+    const unsigned bal = __ballot_sync(0xffffffffu, m);
+    if (lane == 0) red[warp] = __popc(bal);
+    __syncthreads();
+    uint32_t before = 0, total = 0;
+    for (int q = 0; q < NW; ++q) {
+      const uint32_t c = static_cast<uint32_t>(red[q]);
+      if (q < warp) before += c;
+      total += c;
+    }
+    const int64_t rank = running + before + __popc(bal & ((1u << lane) - 1u));
+    if (m && rank % nw == w) {
+      const int64_t slot = rank / nw;
+      if (slot < kMaxRowList) list[slot] = static_cast<int32_t>(row);
+    }
+    running += total;
+    __syncthreads();
+  }
+  if (running > w) count = static_cast<int>((running - 1 - w) / nw + 1);
+  return count < kMaxRowList ? count : kMaxRowList;
+}
 
 // ------------------------------------------------------------------------------------------
 // Shared-memory layout (identical on host and device).
 // ------------------------------------------------------------------------------------------
 struct Layout {
-  size_t xs, raw, cand_key, cand_idx, hist, fine, sup, small, gmax, red, slots, mbar, misc, total;
+  size_t xs, raw, cand_key, cand_idx, hist, fine, sup, small, gmax, red, slots, mbar, misc, rows, total;
 };
 
 __host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
@@ -129,15 +176,17 @@ __host__ __device__ inline Layout make_layout(int nc, bool bf16) {
   L.raw = off;      off += bf16 ? align16(size_t(nc) * 2) : 0;
   L.cand_key = off; off += size_t(kCapLoc) * 4;  // also the penalty bitmap (nc/8 bytes)
   L.cand_idx = off; off += size_t(kCapLoc) * 4;
-  L.hist = off;     off += size_t(kLinBins) * 8;  // also the gathered group maxima
-  L.fine = off;     off += size_t(kFineBins) * 8;
-  L.sup = off;      off += size_t(kLinBins / 32 + kFineBins / 32) * 8;
+  L.hist = off;     off += size_t(3 * 1024) * 4;  // histograms (u32 counts or 16-bit mass limbs),
+                                                   // also the gathered group maxima
+  L.fine = off;     off += size_t(3 * kFineBins) * 4;
+  L.sup = off;      off += size_t(kLinBinsP / 32 + kFineBins / 32) * 8;
   L.small = off;    off += size_t(2 * kSmall) * 8;  // own boundary list, then the gathered one
   L.gmax = off;     off += align16(size_t((nc + 127) / 128) * 4);
   L.red = off;      off += 40 * 8;
   L.slots = off;    off += size_t(kNumSlots) * 8;
   L.mbar = off;     off += 16;
   L.misc = off;     off += 16 * 8;
+  L.rows = off;     off += size_t(kMaxRowList) * 4;
   L.total = off;
   return L;
 }
@@ -191,18 +240,18 @@ __device__ __forceinline__ int lin_bin_scaled(float y, float M, float s, int nb)
   if (!(f < static_cast<float>(nb))) return nb - 1;
   return static_cast<int>(f);
 }
-// First histogram of top-p-only rows: bins of width 1/32 in d = M - x over
-// [0, 64); returns kLinBins for d >= 64 (zero fixed-point mass).
+// First histogram of top-p-only rows: bins of width 1/16 in d = M - x over
+// [0, 64); returns kLinBinsP for d >= 64 (zero fixed-point mass).
 __device__ __forceinline__ int lin_bin_mass(float x, float M) {
   if (x == M) return 0;
   const float d = __fsub_rn(M, x);
-  if (!(d < 64.0f)) return kLinBins;
-  return static_cast<int>(d * 32.0f);
+  if (!(d < 64.0f)) return kLinBinsP;
+  return static_cast<int>(d * 16.0f);
 }
-// Refinement inside first-level bin b: kFineBins bins over d in [b/32, (b+1)/32).
+// Refinement inside first-level bin b: kFineBins bins over d in [b/16, (b+1)/16).
 __device__ __forceinline__ int fine_bin_mass(float x, float M, int b) {
   const float d = (x == M) ? 0.0f : __fsub_rn(M, x);
-  const float f = __fmul_rn(__fsub_rn(d, static_cast<float>(b) * 0.03125f), 32.0f * kFineBins);
+  const float f = __fmul_rn(__fsub_rn(d, static_cast<float>(b) * 0.0625f), 16.0f * kFineBins);
   if (!(f > 0.0f)) return 0;
   if (!(f < static_cast<float>(kFineBins))) return kFineBins - 1;
   return static_cast<int>(f);
@@ -326,17 +375,57 @@ __device__ uint32_t block_excl_scan_u32(uint32_t v, uint32_t* total, unsigned lo
 // Sum over the cluster of the value at the same shared-memory address in
 // every CTA (loads issued together).
 template <typename T>
-__device__ __forceinline__ T remote_sum(cg::cluster_group& cl, T* p, int CS) {
-  T s = T(0);
+__device__ __forceinline__ unsigned long long remote_sum(cg::cluster_group& cl, T* p, int CS) {
+  unsigned long long s = 0;
   for (int r = 0; r < CS; r += 4) {
     T v[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) v[u] = r + u < CS ? *cl.map_shared_rank(p, r + u) : T(0);
 #pragma unroll
-    for (int u = 0; u < 4; ++u) s += v[u];
+    for (int u = 0; u < 4; ++u) s += static_cast<unsigned long long>(v[u]);
   }
   return s;
 }
+
+// A histogram of nb bins in shared memory.  L = 1: u32 counts.  L = 3: a fixed-point
+// mass split into three 16-bit limbs, one u32 array each (shared-memory 64-bit atomics
+// are slow; 32-bit ones are not).  A bin may take up to 65536 additions without a limb
+// overflowing, so the exact u64 sum is limb0 + (limb1 << 16) + (limb2 << 32).
+template <int L>
+struct Bins {
+  uint32_t* base;
+  int nb;
+  __device__ __forceinline__ void clear(int nthreads) const {
+    for (int i = threadIdx.x; i < L * nb; i += nthreads) base[i] = 0u;
+  }
+  __device__ __forceinline__ void add(int b, unsigned long long w) const {
+    if (L == 1) {
+      atomicAdd(base + b, static_cast<uint32_t>(w));
+    } else {
+      atomicAdd(base + b, static_cast<uint32_t>(w & 0xFFFFu));
+      atomicAdd(base + nb + b, static_cast<uint32_t>((w >> 16) & 0xFFFFu));
+      atomicAdd(base + 2 * nb + b, static_cast<uint32_t>(w >> 32));
+    }
+  }
+  __device__ __forceinline__ unsigned long long get(int b) const {
+    if (L == 1) return base[b];
+    return static_cast<unsigned long long>(base[b]) + (static_cast<unsigned long long>(base[nb + b]) << 16) +
+           (static_cast<unsigned long long>(base[2 * nb + b]) << 32);
+  }
+  // the same bin of CTA r of the cluster
+  __device__ __forceinline__ unsigned long long get_rank(cg::cluster_group& cl, int b, int r) const {
+    const uint32_t* rb = cl.map_shared_rank(base, r);
+    if (L == 1) return rb[b];
+    return static_cast<unsigned long long>(rb[b]) + (static_cast<unsigned long long>(rb[nb + b]) << 16) +
+           (static_cast<unsigned long long>(rb[2 * nb + b]) << 32);
+  }
+  // the bin summed over the cluster (loads issued together)
+  __device__ __forceinline__ unsigned long long get_cluster(cg::cluster_group& cl, int b, int CS) const {
+    unsigned long long s = 0;
+    for (int l = 0; l < L; ++l) s += remote_sum(cl, base + l * nb + b, CS) << (16 * l);
+    return s;
+  }
+};
 
 // Pushes a u64 into slot array `arr` (index = own rank) of every CTA of the cluster.
 __device__ __forceinline__ void push_all(cg::cluster_group& cl, unsigned long long* arr, int rank, int CS,
@@ -360,8 +449,8 @@ struct Ctx {
   float M;              // row maximum (transformed)
   uint32_t* cand_key;   // candidate list of this CTA (transformed keys)
   int32_t* cand_idx;
-  unsigned long long* hist;  // kLinBins u64 (fallback radix uses two 256-bin halves)
-  unsigned long long* fine;  // kFineBins u64
+  uint32_t* hist;            // 3072 words: 2048 counts, 1024-bin limb histogram, or radix bins
+  uint32_t* fine;            // 3 x kFineBins words: 1024-bin limb histogram
   unsigned long long* sup;   // kLinBins/32 + kFineBins/32 u64 (fallback radix uses two 16-entry halves)
   unsigned long long* small; // [kSmall] own boundary list, [kSmall] gathered list
   uint32_t* gmax;            // this CTA's group maxima (raw keys)
@@ -479,6 +568,7 @@ __device__ int32_t nth_tie(const SrcCand& s, const Ctx& c, uint32_t tkey, uint32
 template <class Src, bool kMass>
 __device__ Thresh radix_select(cg::cluster_group& cl, Ctx& c, const Src& src, unsigned long long target,
                                bool p_mode, float p, uint32_t rk, int32_t ri) {
+  constexpr int L = kMass ? 3 : 1;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int CS = static_cast<int>(cl.num_blocks());
   uint32_t prefix = 0, pmask = 0;
@@ -488,9 +578,9 @@ __device__ Thresh radix_select(cg::cluster_group& cl, Ctx& c, const Src& src, un
   int cur = 0;
   for (int d = 0; d < 4; ++d) {
     const int shift = 24 - 8 * d;
-    unsigned long long* h = c.hist + cur * kBins;
+    const Bins<L> h{c.hist + cur * 3 * kBins, kBins};
     unsigned long long* s = c.sup + cur * kSuper;
-    for (int i = threadIdx.x; i < kBins; i += kThreads) h[i] = 0ull;
+    h.clear(kThreads);
     __syncthreads();
     src.for_each([&](bool valid, uint32_t key, int32_t idx, float x) {
       const bool take = valid && (key & pmask) == prefix && kept_by(key, idx, rk, ri);
@@ -498,16 +588,15 @@ __device__ Thresh radix_select(cg::cluster_group& cl, Ctx& c, const Src& src, un
       if (kMass) {
         if (take) {
           const unsigned long long w = fixed_mass(softmax_weight(x, c.M));
-          if (w) atomicAdd(&h[bin], w);
+          if (w) h.add(bin, w);
         }
       } else {
-        const unsigned peers = __match_any_sync(kFull, take ? bin : -1);
-        if (take && lane == __ffs(peers) - 1) atomicAdd(&h[bin], static_cast<unsigned long long>(__popc(peers)));
+        if (take) h.add(bin, 1ull);
       }
     });
     __syncthreads();
     if (threadIdx.x < kBins) {
-      unsigned long long v = h[threadIdx.x];
+      unsigned long long v = h.get(threadIdx.x);
 #pragma unroll
       for (int o = 8; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
       if ((threadIdx.x & 15) == 0) s[threadIdx.x >> 4] = v;
@@ -532,10 +621,10 @@ __device__ Thresh radix_select(cg::cluster_group& cl, Ctx& c, const Src& src, un
       int beta = 0;
       bool good = (m != 0u) && tau > 0;
       if (good) {
-        const int L = __ffs(m) - 1;
-        const unsigned long long above = L > 0 ? __shfl_sync(kFull, inc, L - 1) : 0ull;
-        const int sigma = kSuper - 1 - L;
-        const unsigned long long bv = lane < 16 ? remote_sum(cl, h + sigma * 16 + (15 - (lane & 15)), CS) : 0ull;
+        const int L0 = __ffs(m) - 1;
+        const unsigned long long above = L0 > 0 ? __shfl_sync(kFull, inc, L0 - 1) : 0ull;
+        const int sigma = kSuper - 1 - L0;
+        const unsigned long long bv = lane < 16 ? h.get_cluster(cl, sigma * 16 + (15 - (lane & 15)), CS) : 0ull;
         const unsigned long long inc2 = warp_incl_scan_u64(bv, lane);
         const unsigned m2 = __ballot_sync(kFull, lane < 16 && above + inc2 >= tau);
         if (m2 == 0u) {
@@ -580,17 +669,18 @@ __device__ Thresh radix_select(cg::cluster_group& cl, Ctx& c, const Src& src, un
   // (the last pass's local histograms, still intact).
   const int last = cur ^ 1;
   const int beta_last = static_cast<int>(key & 0xFFu);
+  const Bins<L> hl{c.hist + last * 3 * kBins, kBins};
   if (warp == 0) {
     unsigned long long t = 0;
-    if (lane < CS) t = *cl.map_shared_rank(c.hist + last * kBins + beta_last, lane) / w1;
+    if (lane < CS) t = hl.get_rank(cl, beta_last, lane) / w1;
     const unsigned long long inc = warp_incl_scan_u64(t, lane);
     const unsigned m = __ballot_sync(kFull, lane < CS && inc >= need);
     int owner = -1;
     unsigned long long jloc = 0;
     if (m) {
-      const int L = __ffs(m) - 1;
-      const unsigned long long before = L > 0 ? __shfl_sync(kFull, inc, L - 1) : 0ull;
-      owner = L;
+      const int L0 = __ffs(m) - 1;
+      const unsigned long long before = L0 > 0 ? __shfl_sync(kFull, inc, L0 - 1) : 0ull;
+      owner = L0;
       jloc = need - before;
     }
     if (lane == 0) {
@@ -619,7 +709,7 @@ __device__ Thresh radix_select(cg::cluster_group& cl, Ctx& c, const Src& src, un
 // Uses the first 256 words of hist as a count histogram.
 __device__ uint32_t local_kth_largest(Ctx& c, const uint32_t* keys, int n, uint32_t k, int passes) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t* h = reinterpret_cast<uint32_t*>(c.hist);
+  uint32_t* h = c.hist;
   uint32_t prefix = 0, pmask = 0;
   for (int d = 0; d < passes; ++d) {
     const int shift = 24 - 8 * d;
@@ -685,12 +775,12 @@ struct Boundary {
   unsigned long long binw;  // weight of bin beta
   unsigned long long tau;   // target used
 };
-__device__ Boundary find_boundary(cg::cluster_group& cl, Ctx& c, unsigned long long* h,
-                                  unsigned long long* sup, int nb, unsigned long long tau, bool p_mode,
-                                  float p) {
+template <int L>
+__device__ Boundary find_boundary(cg::cluster_group& cl, Ctx& c, const Bins<L>& h, unsigned long long* sup,
+                                  unsigned long long tau, bool p_mode, float p) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int CS = static_cast<int>(cl.num_blocks());
-  const int nsup = nb / 32;
+  const int nsup = h.nb / 32;
   if (warp == 0) {
     const int i0 = 2 * lane, i1 = 2 * lane + 1;
     const unsigned long long s0 = i0 < nsup ? remote_sum(cl, sup + (i0 < nsup ? i0 : 0), CS) : 0ull;
@@ -713,7 +803,7 @@ __device__ Boundary find_boundary(cg::cluster_group& cl, Ctx& c, unsigned long l
       const unsigned long long s0L = __shfl_sync(kFull, s0, Ls);
       const int sigma = (before + s0L >= tau) ? 2 * Ls : 2 * Ls + 1;
       const unsigned long long abv = (sigma == 2 * Ls) ? before : before + s0L;
-      const unsigned long long bv = remote_sum(cl, h + sigma * 32 + lane, CS);
+      const unsigned long long bv = h.get_cluster(cl, sigma * 32 + lane, CS);
       const unsigned long long inc2 = warp_incl_scan_u64(bv, lane);
       const unsigned m2 = __ballot_sync(kFull, abv + inc2 >= tau);
       if (m2) {
@@ -740,10 +830,11 @@ __device__ Boundary find_boundary(cg::cluster_group& cl, Ctx& c, unsigned long l
   return b;
 }
 
-// Super sums of 32 bins (nb bins in h) into sup; block-wide, before cl.sync.
-__device__ __forceinline__ void super_sums(const unsigned long long* h, unsigned long long* sup, int nb) {
-  for (int t = threadIdx.x; t < nb / 4; t += kThreads) {
-    unsigned long long v = h[4 * t] + h[4 * t + 1] + h[4 * t + 2] + h[4 * t + 3];
+// Super sums of 32 bins into sup; block-wide, before cl.sync.
+template <int L>
+__device__ __forceinline__ void super_sums(const Bins<L>& h, unsigned long long* sup) {
+  for (int t = threadIdx.x; t < h.nb / 4; t += kThreads) {
+    unsigned long long v = h.get(4 * t) + h.get(4 * t + 1) + h.get(4 * t + 2) + h.get(4 * t + 3);
     v += __shfl_xor_sync(kFull, v, 1);
     v += __shfl_xor_sync(kFull, v, 2);
     v += __shfl_xor_sync(kFull, v, 4);
@@ -843,8 +934,8 @@ __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P)
   c.n4 = n4;
   c.cand_key = reinterpret_cast<uint32_t*>(smem + L.cand_key);
   c.cand_idx = reinterpret_cast<int32_t*>(smem + L.cand_idx);
-  c.hist = reinterpret_cast<unsigned long long*>(smem + L.hist);
-  c.fine = reinterpret_cast<unsigned long long*>(smem + L.fine);
+  c.hist = reinterpret_cast<uint32_t*>(smem + L.hist);
+  c.fine = reinterpret_cast<uint32_t*>(smem + L.fine);
   c.sup = reinterpret_cast<unsigned long long*>(smem + L.sup);
   c.small = reinterpret_cast<unsigned long long*>(smem + L.small);
   c.gmax = reinterpret_cast<uint32_t*>(smem + L.gmax);
@@ -860,7 +951,8 @@ __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P)
     if (tma && threadIdx.x == 0) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       mbar_expect_tx(mbar, bytes);
-      constexpr uint32_t kPiece = 16384;
+      // one bulk copy per chunk: a copy's cost is mostly fixed, not proportional to its size
+      constexpr uint32_t kPiece = 1u << 20;
       const unsigned char* src = gsrc_of(row);
       for (uint32_t off = 0; off < bytes; off += kPiece) {
         const uint32_t len = bytes - off < kPiece ? bytes - off : kPiece;
@@ -869,14 +961,27 @@ __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P)
     }
   };
 
+  // the rows this cluster owns (every CTA of the cluster computes the same list)
+  int32_t* rowlist = reinterpret_cast<int32_t*>(smem + L.rows);
+  int my_rows = 0;
+  if (P.filter == 0) {
+    my_rows = P.B > cid ? static_cast<int>((P.B - 1 - cid) / ncl + 1) : 0;
+  } else {
+    my_rows = build_row_list<kThreads>(P, cid, ncl, rowlist, c.red);
+  }
+  auto row_at = [&](int i) -> int64_t {
+    return P.filter == 0 ? cid + static_cast<int64_t>(i) * ncl : static_cast<int64_t>(rowlist[i]);
+  };
+
   if (threadIdx.x == 0) mbar_init(mbar, 1);
   __syncthreads();
-  if (cid < P.B) issue_load(cid);
+  if (my_rows > 0) issue_load(row_at(0));
   bool timed_out = false;
   uint32_t parity = 0;
 
-  for (int64_t row = cid; row < P.B; row += ncl, parity ^= 1u) {
-    const int64_t next = row + ncl;
+  for (int ri = 0; ri < my_rows; ++ri, parity ^= 1u) {
+    const int64_t row = row_at(ri);
+    const int64_t next = ri + 1 < my_rows ? row_at(ri + 1) : -1;
     bool next_issued = false;
 
     // ---- row parameters (uniform across the cluster) ---------------------------------
@@ -1067,7 +1172,8 @@ __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P)
         const float s = (span > 0.0f && span < INFINITY) ? __fdiv_rn(static_cast<float>(kLinBins), span) : 0.0f;
         // candidate pass: count histogram over linear bins of (M - y)
         __syncthreads();  // gall (inside hist) is dead from here
-        for (int i = threadIdx.x; i < kLinBins; i += kThreads) c.hist[i] = 0ull;
+        const Bins<1> hk{c.hist, kLinBins};
+        hk.clear(kThreads);
         if (threadIdx.x == 0) sh_cnt = 0u;
         __syncthreads();
         const float4* x4 = reinterpret_cast<const float4*>(xs);
@@ -1087,7 +1193,7 @@ __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P)
                   ck[e] = ky;
                   ++cnt;
                   const int b = s > 0.0f ? lin_bin_scaled(y, M, s, kLinBins) : 0;
-                  atomicAdd(&c.hist[b], 1ull);
+                  hk.add(b, 1ull);
                 }
               }
             }
@@ -1116,12 +1222,12 @@ __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P)
         if (orow) write_neg_inf();
         __syncthreads();
         ncand = static_cast<int>(sh_cnt);
-        super_sums(c.hist, c.sup, kLinBins);
+        super_sums(hk, c.sup);
         if (threadIdx.x == 0) push_all(cl, c.slots + kSlotFlag, rank, CS, ncand <= kCapLoc ? 1ull : 0ull);
         cl.sync();
         bool lists_ok = true;
         for (int r = 0; r < CS; ++r) lists_ok = lists_ok && c.slots[kSlotFlag + r] != 0ull;
-        const Boundary bk = find_boundary(cl, c, c.hist, c.sup, kLinBins, static_cast<unsigned long long>(k), false, 0.0f);
+        const Boundary bk = find_boundary(cl, c, hk, c.sup, static_cast<unsigned long long>(k), false, 0.0f);
         fast = lists_ok && bk.beta >= 0 && bk.binw <= static_cast<unsigned long long>(kSmall);
         if (fast) {
           // the k-th element lies in bin beta: rank that bin's elements exactly
@@ -1147,7 +1253,7 @@ __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P)
           if (fast) {
             // the chunk is no longer needed: start the next row's load now
             __syncthreads();
-            if (next < P.B) {
+            if (next >= 0) {
               issue_load(next);
               next_issued = true;
             }
@@ -1161,7 +1267,8 @@ __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P)
                   (span2 > 0.0f && span2 < INFINITY) ? __fdiv_rn(static_cast<float>(kLinBins), span2) : 0.0f;
               // hist is still read by other CTAs until the next barrier: use `fine` as a
               // 1024-bin histogram (half resolution)
-              for (int i = threadIdx.x; i < kFineBins; i += kThreads) c.fine[i] = 0ull;
+              const Bins<3> hm{c.fine, kFineBins};
+              hm.clear(kThreads);
               __syncthreads();
               for (int i = threadIdx.x; i < ncand; i += kThreads) {
                 const uint32_t key = c.cand_key[i];
@@ -1169,12 +1276,12 @@ __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P)
                 const float y = kfloat(key);
                 const int b = s2 > 0.0f ? (lin_bin_scaled(y, M, s2, kLinBins) >> 1) : 0;
                 const unsigned long long w = fixed_mass(softmax_weight(y, M));
-                if (w) atomicAdd(&c.fine[b], w);
+                if (w) hm.add(b, w);
               }
               __syncthreads();
-              super_sums(c.fine, c.sup, kFineBins);
+              super_sums(hm, c.sup);
               cl.sync();
-              const Boundary bp = find_boundary(cl, c, c.fine, c.sup, kFineBins, 0ull, true, p);
+              const Boundary bp = find_boundary(cl, c, hm, c.sup, 0ull, true, p);
               bool ok2 = bp.beta >= 0;
               if (ok2) {
                 if (threadIdx.x == 0) sh_cnt = 0u;
@@ -1221,8 +1328,8 @@ __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P)
     } else if (topp_on) {
       // ---- top-p over the whole row ----------------------------------------------
       transform_in_place();
-      unsigned long long* h = c.hist;
-      for (int i = threadIdx.x; i < kLinBins; i += kThreads) h[i] = 0ull;
+      const Bins<3> h{c.hist, kLinBinsP};
+      h.clear(kThreads);
       __syncthreads();
       const float4* x4 = reinterpret_cast<const float4*>(xs);
       for (int g = threadIdx.x; g < n4; g += kThreads) {
@@ -1232,21 +1339,22 @@ __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P)
         for (int e = 0; e < 4; ++e) {
           if (fkey(vv[e]) == 0u) continue;
           const int b = lin_bin_mass(vv[e], M);
-          if (b < kLinBins) {
+          if (b < kLinBinsP) {
             const unsigned long long w = fixed_mass(softmax_weight(vv[e], M));
-            if (w) atomicAdd(&h[b], w);
+            if (w) h.add(b, w);
           }
         }
       }
       __syncthreads();
-      super_sums(h, c.sup, kLinBins);
+      super_sums(h, c.sup);
       cl.sync();
-      const Boundary b1 = find_boundary(cl, c, h, c.sup, kLinBins, 0ull, true, p);
+      const Boundary b1 = find_boundary(cl, c, h, c.sup, 0ull, true, p);
       bool ok = b1.beta >= 0;
       Boundary b2{-1, 0, 0, 0};
       if (ok) {
         // finer histogram inside bin beta (into `fine`; hist is still being read)
-        for (int i = threadIdx.x; i < kFineBins; i += kThreads) c.fine[i] = 0ull;
+        const Bins<3> hf{c.fine, kFineBins};
+        hf.clear(kThreads);
         __syncthreads();
         for (int g = threadIdx.x; g < n4; g += kThreads) {
           const float4 v = x4[g];
@@ -1255,16 +1363,16 @@ __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P)
           for (int e = 0; e < 4; ++e) {
             if (fkey(vv[e]) == 0u || lin_bin_mass(vv[e], M) != b1.beta) continue;
             const unsigned long long w = fixed_mass(softmax_weight(vv[e], M));
-            if (w) atomicAdd(&c.fine[fine_bin_mass(vv[e], M, b1.beta)], w);
+            if (w) hf.add(fine_bin_mass(vv[e], M, b1.beta), w);
           }
         }
         __syncthreads();
         // super sums go to the second half of sup (the first half is still being read)
-        super_sums(c.fine, c.sup + kLinBins / 32, kFineBins);
+        super_sums(hf, c.sup + kLinBinsP / 32);
       }
       cl.sync();
       if (ok) {
-        b2 = find_boundary(cl, c, c.fine, c.sup + kLinBins / 32, kFineBins, b1.tau - b1.above, false, 0.0f);
+        b2 = find_boundary(cl, c, Bins<3>{c.fine, kFineBins}, c.sup + kLinBinsP / 32, b1.tau - b1.above, false, 0.0f);
         ok = b2.beta >= 0;
       }
       if (ok) {
@@ -1398,7 +1506,7 @@ __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P)
 
     // the chunk buffer is free: start the next row's load if it has not started yet
     __syncthreads();
-    if (!next_issued && next < P.B) issue_load(next);
+    if (!next_issued && next >= 0) issue_load(next);
   }
 
   // a CTA that gave up on a copy waits (bounded) for it before leaving
@@ -1407,6 +1515,8 @@ __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P)
   cl.sync();
 }
 
+
+#include "kps_stream.cuh"
 
 // ------------------------------------------------------------------------------------------
 // Host side
@@ -1536,6 +1646,128 @@ static kps_status choose_launch(int64_t B, int64_t V, LaunchCfg* out) {
   return KPS_OK;
 }
 
+// Kernel choice: 0 = automatic, 1 = cluster kernel only, 2 = streaming kernel where supported.
+static int g_policy = 0;
+constexpr int64_t kStreamMinRows = 64;  // automatic: the streaming kernel from this batch size up
+
+struct StreamCfg {
+  int stages;
+  size_t smem;
+  int ctas;
+};
+
+template <bool kBF16>
+static cudaError_t prepare_stream_kernel() {
+  static std::mutex mu;
+  static bool done[64] = {};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[dev]) return cudaSuccess;
+  cudaFuncAttributes fa;
+  err = cudaFuncGetAttributes(&fa, kps_stream_kernel<kBF16>);
+  if (err != cudaSuccess) return err;
+  const int optin = device_smem_optin() - static_cast<int>(fa.sharedSizeBytes);
+  err = cudaFuncSetAttribute(kps_stream_kernel<kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+  if (err == cudaSuccess) done[dev] = true;
+  return err;
+}
+
+// Ring depth and grid of the streaming kernel; false if it cannot run this shape.
+template <bool kBF16>
+static bool choose_stream(int64_t B, int64_t V, StreamCfg* out) {
+  if (V > kSMaxV) return false;
+  if (prepare_stream_kernel<kBF16>() != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, kps_stream_kernel<kBF16>) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  const int optin = device_smem_optin() - static_cast<int>(fa.sharedSizeBytes);
+  const SLayout base = make_slayout(V, kBF16, 0);
+  if (static_cast<size_t>(optin) <= base.total) return false;
+  int stages = static_cast<int>((static_cast<size_t>(optin) - base.total) / base.stage_bytes);
+  if (stages > kSMaxStages) stages = kSMaxStages;
+  if (stages < kSMinStages) return false;
+  const size_t smem = make_slayout(V, kBF16, stages).total;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kps_stream_kernel<kBF16>, kSThreads, smem) != cudaSuccess ||
+      per_sm < 1) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  const int64_t slots = static_cast<int64_t>(device_sm_count()) * per_sm;
+  out->stages = stages;
+  out->smem = smem;
+  out->ctas = static_cast<int>(B < slots ? B : slots);
+  return true;
+}
+
+// Launch decisions depend only on (device, dtype, V) plus min() with B, so they are
+// computed once and cached: kps_sample then costs one lookup and one launch.
+struct CachedShape {
+  int dev;
+  int dt;
+  int64_t V;
+  bool stream_ok;
+  StreamCfg stream;
+  int64_t stream_slots;  // resident CTAs of the streaming kernel
+  bool cluster_ok;
+  kps_status cluster_status;
+  LaunchCfg cluster;      // clusters = resident clusters (min with B at launch)
+  bool cluster_small_b;   // cluster choice was made for a batch smaller than the SM count
+};
+
+static kps_status lookup_shape(kps_dtype dt, int64_t V, int64_t B, bool want_stream, CachedShape* out) {
+  static std::mutex mu;
+  static CachedShape cache[32];
+  static int used = 0, next = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return KPS_ERR_CUDA;
+  }
+  // the cluster size depends on whether the batch fills the SMs (small batches widen clusters)
+  const bool small_b = B * 2 <= device_sm_count();
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < used; ++i) {
+    const CachedShape& c = cache[i];
+    if (c.dev == dev && c.dt == static_cast<int>(dt) && c.V == V && c.cluster_small_b == small_b) {
+      *out = c;
+      return KPS_OK;
+    }
+  }
+  CachedShape c{};
+  c.dev = dev;
+  c.dt = static_cast<int>(dt);
+  c.V = V;
+  c.cluster_small_b = small_b;
+  (void)want_stream;
+  const int64_t bigB = 1 << 20;
+  StreamCfg sc{};
+  c.stream_ok = dt == KPS_BF16 ? choose_stream<true>(bigB, V, &sc) : choose_stream<false>(bigB, V, &sc);
+  c.stream = sc;
+  c.stream_slots = c.stream_ok ? sc.ctas : 0;
+  LaunchCfg lc{};
+  const int64_t probeB = small_b ? B : bigB;
+  c.cluster_status = dt == KPS_BF16 ? choose_launch<true>(probeB, V, &lc) : choose_launch<false>(probeB, V, &lc);
+  c.cluster_ok = c.cluster_status == KPS_OK;
+  c.cluster = lc;
+  if (used < 32) {
+    cache[used++] = c;
+  } else {
+    cache[next] = c;
+    next = (next + 1) % 32;
+  }
+  *out = c;
+  return KPS_OK;
+}
+
 }  // namespace kps
 
 // ------------------------------------------------------------------------------------------
@@ -1603,10 +1835,25 @@ kps_status kps_sample(const void* logits, kps_dtype dt, int64_t B, int64_t V, co
   if (need_logits && !out_filtered) return KPS_ERR_INVALID_ARG;
   const bool pen = seen_indptr && seen_ids && penalty;
 
+  const size_t esize = dt == KPS_BF16 ? 2 : 4;
+  const bool aligned = (reinterpret_cast<uintptr_t>(logits) % 16 == 0) && ((V * esize) % 16 == 0) &&
+                       (reinterpret_cast<uintptr_t>(q) % 16 == 0) && (V % 4 == 0) &&
+                       (!need_logits || reinterpret_cast<uintptr_t>(out_filtered) % 16 == 0);
+  const bool want_stream =
+      aligned && (kps::g_policy == 2 || (kps::g_policy == 0 && B >= kps::kStreamMinRows));
+  kps::StreamCfg scfg;
   kps::LaunchCfg cfg;
-  const kps_status st =
-      dt == KPS_BF16 ? kps::choose_launch<true>(B, V, &cfg) : kps::choose_launch<false>(B, V, &cfg);
-  if (st != KPS_OK) return st;
+  bool use_stream = false;
+  {
+    kps::CachedShape cs;
+    const kps_status st = kps::lookup_shape(dt, V, B, want_stream, &cs);
+    if (st != KPS_OK) return st;
+    use_stream = want_stream && cs.stream_ok;
+    scfg = cs.stream;
+    scfg.ctas = static_cast<int>(B < cs.stream_slots ? B : cs.stream_slots);
+    cfg = cs.cluster;
+    if (!use_stream && !cs.cluster_ok) return cs.cluster_status;
+  }
 
   kps::Params P;
   P.logits = logits;
@@ -1625,11 +1872,34 @@ kps_status kps_sample(const void* logits, kps_dtype dt, int64_t B, int64_t V, co
   P.out_filtered = need_logits ? out_filtered : nullptr;
   P.status = static_cast<int*>(workspace);
   P.nc = cfg.nc;
-  const size_t esize = dt == KPS_BF16 ? 2 : 4;
-  const bool aligned = (reinterpret_cast<uintptr_t>(logits) % 16 == 0) && ((V * esize) % 16 == 0) &&
-                       (reinterpret_cast<uintptr_t>(q) % 16 == 0) && (V % 4 == 0) &&
-                       (!need_logits || reinterpret_cast<uintptr_t>(out_filtered) % 16 == 0);
   P.use_tma = aligned ? 1 : 0;
+  P.filter = 0;
+
+  // Automatic mode splits the batch: the streaming kernel takes the top-k and
+  // one-element rows (one HBM pass each, one SM per row), then the cluster kernel
+  // takes the rest (top-p over the whole row, or every element kept), whose
+  // per-element softmax work is spread over a cluster of SMs per row.
+  const int64_t cl_workers = B < cfg.clusters ? B : cfg.clusters;
+  const bool split = use_stream && kps::g_policy == 0 && cfg.clusters > 0 &&
+                     B <= static_cast<int64_t>(kps::kMaxRowList) * scfg.ctas &&
+                     B <= static_cast<int64_t>(kps::kMaxRowList) * cl_workers;
+  if (use_stream) {
+    cudaLaunchConfig_t sl = {};
+    sl.gridDim = dim3(static_cast<unsigned>(scfg.ctas));
+    sl.blockDim = dim3(kps::kSThreads);
+    sl.dynamicSmemBytes = scfg.smem;
+    sl.stream = stream;
+    const int stages = scfg.stages;
+    P.filter = split ? 1 : 0;
+    cudaError_t e = dt == KPS_BF16 ? cudaLaunchKernelEx(&sl, kps::kps_stream_kernel<true>, P, stages)
+                                   : cudaLaunchKernelEx(&sl, kps::kps_stream_kernel<false>, P, stages);
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();
+      return KPS_ERR_CUDA;
+    }
+    if (!split) return KPS_OK;
+    P.filter = 2;
+  }
 
   cudaLaunchConfig_t lc = {};
   const int64_t clusters = B < cfg.clusters ? B : cfg.clusters;  // persistent: clusters walk the rows
@@ -1652,6 +1922,14 @@ kps_status kps_sample(const void* logits, kps_dtype dt, int64_t B, int64_t V, co
   }
   return KPS_OK;
 }
+
+kps_status kps_set_kernel_policy(int policy) {
+  if (policy < 0 || policy > 2) return KPS_ERR_INVALID_ARG;
+  kps::g_policy = policy;
+  return KPS_OK;
+}
+
+int kps_get_kernel_policy(void) { return kps::g_policy; }
 
 kps_status kps_last_device_status(void* workspace, cudaStream_t stream, int* out) {
   if (!workspace || !out) return KPS_ERR_INVALID_ARG;

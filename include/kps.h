@@ -143,6 +143,19 @@ kps_status kps_sample_noalloc(const void* logits, kps_dtype dt, int64_t B, int64
                               const float* penalty, const float* q, float eps, int need_logits,
                               int64_t* out_idx, float* out_filtered, cudaStream_t stream);
 
+/* Kernel selection, process-wide (for tests and tuning):
+ *   0 = automatic (default): the streaming kernel — one CTA per row at a
+ *       time, each row streamed once through a TMA ring — for batches of at
+ *       least 64 rows whose rows are 16-byte aligned and V <= 262144; the
+ *       cluster kernel — one thread-block cluster per row, the row resident
+ *       in the cluster's shared memory — otherwise;
+ *   1 = always the cluster kernel;
+ *   2 = the streaming kernel whenever the shape allows it.
+ * Both compute the same results.  Not thread-safe against concurrent
+ * kps_sample calls. */
+kps_status kps_set_kernel_policy(int policy);
+int kps_get_kernel_policy(void);
+
 /* Static description of a status code. */
 const char* kps_status_string(kps_status s);
 

@@ -28,36 +28,48 @@ def _built():
     oracle.build()
 
 
+@pytest.fixture(params=["cluster", "stream", "auto"])
+def kernel(request):
+    """Runs the test under each kernel policy: the cluster kernel alone, the streaming
+    kernel alone (it only takes aligned rows; other shapes fall back to the cluster
+    kernel), and the automatic split of one batch between the two."""
+    import decode_token_sampling_gb300 as kps
+    kps.set_kernel_policy({"cluster": kps.KERNEL_CLUSTER, "stream": kps.KERNEL_STREAM,
+                           "auto": kps.KERNEL_AUTO}[request.param])
+    yield request.param
+    kps.set_kernel_policy(kps.KERNEL_AUTO)
+
+
 @pytest.mark.parametrize("name", WORKLOADS)
-def test_named_workloads(name):
+def test_named_workloads(name, kernel):
     inp = make_workload(name)
     ref = oracle.sample(inp)
     gi, gf = run_gpu(inp)
-    compare(inp, ref, gi, gf, name)
+    compare(inp, ref, gi, gf, f"{name} [{kernel}]")
     if not inp.need_logits:  # also check the filtered output of the same workload
         ref = oracle.sample(inp, need_logits=True)
         gi, gf = run_gpu(inp, need_logits=True)
-        compare(inp, ref, gi, gf, name + "+logits")
+        compare(inp, ref, gi, gf, f"{name}+logits [{kernel}]")
 
 
-@pytest.mark.parametrize("V", [1, 2, 7, 31, 33, 1023, 1025, 4099, 8191, 40000])
+@pytest.mark.parametrize("V", [1, 2, 7, 31, 33, 1023, 1025, 4099, 8191, 8192, 40000, 40960])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_ragged_vocab(V, dtype):
+def test_ragged_vocab(V, dtype, kernel):
     inp = make_random(6, V, seed=V, dtype=dtype, penalty=1.3, n_seen=min(3 * V, 200))
     ref = oracle.sample(inp)
     gi, gf = run_gpu(inp)
     compare(inp, ref, gi, gf, f"V={V} {dtype}")
 
 
-@pytest.mark.parametrize("V", [64, 5000, 70001])
-def test_ties_and_specials(V):
+@pytest.mark.parametrize("V", [64, 5000, 70001, 70000])
+def test_ties_and_specials(V, kernel):
     inp = make_random(12, V, seed=7 + V, ties=True, special=True, penalty=1.5, n_seen=50)
     ref = oracle.sample(inp)
     gi, gf = run_gpu(inp)
     compare(inp, ref, gi, gf, f"ties V={V}")
 
 
-def test_all_equal_rows_split_ties_by_index():
+def test_all_equal_rows_split_ties_by_index(kernel):
     inp = make_random(8, 3000, seed=11)
     inp.logits[:] = 0.5
     inp.top_k[:] = [1, 2, 17, 1024, 0, 0, 700, 3000][:8]
@@ -68,7 +80,7 @@ def test_all_equal_rows_split_ties_by_index():
     compare(inp, ref, gi, gf, "all-equal")
 
 
-def test_edge_parameters():
+def test_edge_parameters(kernel):
     B, V = 16, 3001
     inp = make_random(B, V, seed=99, penalty=1.2, n_seen=40)
     inp.top_k[:] = [0, -1, 1, 1024, 1025, V, V + 7, 5, 50, 1, 0, 3, 2, 1000, 7, 9]
@@ -80,7 +92,7 @@ def test_edge_parameters():
     compare(inp, ref, gi, gf, "edge params")
 
 
-def test_q_edge_values():
+def test_q_edge_values(kernel):
     inp = make_random(6, 2048, seed=5)
     inp.q[0, :] = 0.0
     inp.q[1, ::2] = np.inf
@@ -120,3 +132,12 @@ def test_side_stream_and_repeat_determinism():
     b = run_gpu(inp)
     np.testing.assert_array_equal(a[0], b[0])
     np.testing.assert_array_equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("B", [1, 3, 64, 200, 600])
+def test_batch_sizes_and_row_walk(B, kernel):
+    """Persistent grids walk several rows per CTA / cluster when B exceeds the resident slots."""
+    inp = make_random(B, 16384, seed=40 + B, penalty=1.2, n_seen=100)
+    ref = oracle.sample(inp)
+    gi, gf = run_gpu(inp)
+    compare(inp, ref, gi, gf, f"B={B} [{kernel}]")
