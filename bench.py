@@ -35,7 +35,6 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 NOMINAL_HBM_GBS = 8000.0
-KERNEL_NAME = "kps_sample_kernel"
 
 
 def measured_peaks() -> dict:
@@ -48,16 +47,19 @@ def measured_peaks() -> dict:
 
 
 def kernel_source_hash() -> str:
+    """Hash of the CUDA sources and the header (profiles record the one they were taken on)."""
     h = hashlib.sha256()
-    for rel in ("decode_token_sampling_gb300/csrc/kps.cu", "include/kps.h"):
+    csrc = os.path.join("decode_token_sampling_gb300", "csrc")
+    rels = sorted(os.path.join(csrc, f) for f in os.listdir(os.path.join(ROOT, csrc)) if f.endswith((".cu", ".cuh", ".h")))
+    for rel in rels + [os.path.join("include", "kps.h")]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic_per_launch(workload: str):
+def ncu_traffic_per_launch(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on this kernel source."""
-    p = os.path.join(ROOT, "profiles", f"kps_sample_kernel_{workload}.md")
+    p = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     if not os.path.exists(p):
         return None
     txt = open(p).read()
@@ -216,7 +218,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel", default="auto", choices=["auto", "cluster", "stream"],
+    ap.add_argument("--kernel", default="auto", choices=["auto", "cluster", "row"],
                     help="kernel policy (auto picks per shape; both compute the same results)")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -240,7 +242,7 @@ def main():
     torch.cuda.set_device(dev)
     kbuild.build()
     kps.set_kernel_policy({"auto": kps.KERNEL_AUTO, "cluster": kps.KERNEL_CLUSTER,
-                           "stream": kps.KERNEL_STREAM}[args.kernel])
+                           "row": kps.KERNEL_ROW}[args.kernel])
 
     inp = make_workload(args.workload)
     B, V = inp.B, inp.V
@@ -266,6 +268,7 @@ def main():
         for _ in range(args.warmup):
             step()
     stream.synchronize()
+    kernel_name = kps.last_kernel()
 
     # ---- device-resident timed region --------------------------------------------------------
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -316,7 +319,7 @@ def main():
     metric_bytes = inp.metric_bytes()
     peaks = measured_peaks()
     achieved_gbs = alg_bytes / (kernel_ms / 1e3) / 1e9
-    traffic = ncu_traffic_per_launch(args.workload)
+    traffic = ncu_traffic_per_launch(kernel_name, args.workload)
 
     # ---- end to end through the public API: pinned host inputs in, results out ---------------
     h = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
@@ -379,7 +382,7 @@ def main():
         "gpu_launches": args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": traffic,
-                     "peak_source": peaks["source"], "kernel": KERNEL_NAME,
+                     "peak_source": peaks["source"], "kernel": kernel_name,
                      "algorithmic_bytes_per_launch": alg_bytes, "kernel_ms": kernel_ms},
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:

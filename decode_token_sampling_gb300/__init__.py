@@ -55,6 +55,8 @@ def load_library() -> ctypes.CDLL:
     lib.kps_set_kernel_policy.argtypes = [I32]
     lib.kps_get_kernel_policy.restype = I32
     lib.kps_get_kernel_policy.argtypes = []
+    lib.kps_last_kernel.restype = I32
+    lib.kps_last_kernel.argtypes = []
     lib.kps_query_launch.restype = I32
     lib.kps_query_launch.argtypes = [I64, I64, I32, ctypes.POINTER(I32), ctypes.POINTER(I64),
                                      ctypes.POINTER(ctypes.c_size_t)]
@@ -100,11 +102,11 @@ def new_workspace(B: int, V: int, dtype: torch.dtype = torch.float32, device="cu
     return torch.zeros(n, dtype=torch.uint8, device=device)
 
 
-KERNEL_AUTO, KERNEL_CLUSTER, KERNEL_STREAM = 0, 1, 2
+KERNEL_AUTO, KERNEL_CLUSTER, KERNEL_ROW, KERNEL_ROW_EXACT = 0, 1, 2, 3
 
 
 def set_kernel_policy(policy: int) -> None:
-    """Process-wide kernel choice: KERNEL_AUTO, KERNEL_CLUSTER or KERNEL_STREAM (see include/kps.h)."""
+    """Process-wide kernel choice: KERNEL_AUTO, KERNEL_CLUSTER, KERNEL_ROW or KERNEL_ROW_EXACT (see include/kps.h)."""
     st = load_library().kps_set_kernel_policy(int(policy))
     if st != 0:
         raise KpsError(st, "kps_set_kernel_policy")
@@ -112,6 +114,14 @@ def set_kernel_policy(policy: int) -> None:
 
 def get_kernel_policy() -> int:
     return int(load_library().kps_get_kernel_policy())
+
+
+KERNEL_NAMES = {1: "kps_sample_kernel", 2: "kps_row_kernel"}
+
+
+def last_kernel() -> str:
+    """Name of the kernel this thread's most recent launching sample() call used ("" if none)."""
+    return KERNEL_NAMES.get(int(load_library().kps_last_kernel()), "")
 
 
 def query_launch(B: int, V: int, dtype: torch.dtype = torch.float32) -> dict:

@@ -35,7 +35,7 @@ def nvcc() -> str:
 def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None) -> str:
     """Compile libkps.so if it is missing or older than its sources; returns its path."""
     srcs = [HDR] + [os.path.join(PKG, "csrc", f) for f in sorted(os.listdir(os.path.join(PKG, "csrc")))
-                    if f.endswith((".cu", ".cuh"))]
+                    if f.endswith((".cu", ".cuh", ".h"))]
     if not force and os.path.exists(LIB) and all(os.path.getmtime(LIB) >= os.path.getmtime(s) for s in srcs):
         return LIB
     tmp = LIB + f".tmp{os.getpid()}"

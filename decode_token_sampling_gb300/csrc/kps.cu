@@ -49,6 +49,8 @@
 // with the same control flow, so the cluster barriers always complete.
 
 #include "kps.h"
+#include "kps_fixed.h"
+#include "kps_div.h"
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -58,6 +60,7 @@
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+#include <type_traits>
 
 namespace cg = cooperative_groups;
 
@@ -76,7 +79,6 @@ constexpr int kLinBinsP = 1024;     // linear mass bins (width 1/16 of d = max -
 constexpr int kFineBins = 1024;     // linear bins of the refinement histogram (top-p-only rows)
 constexpr int kSmall = 64;          // boundary-bin elements resolved by exact ranking
 constexpr int kMaxChunk = 65536;    // largest per-CTA chunk the layout supports
-constexpr float kFixScale = 1099511627776.0f;  // 2^40: fixed-point unit of softmax mass
 constexpr long long kSpinCycles = 4000000000LL;  // bounded wait (~2 s)
 constexpr int kSmemCap2PerSM = 112 * 1024;  // per-CTA budget for two CTAs per SM
 constexpr unsigned kFull = 0xffffffffu;
@@ -113,6 +115,7 @@ struct Params {
   int nc;       // elements per CTA (multiple of 8)
   int use_tma;  // every row of logits, q and out starts on a 16-byte boundary
   int filter;   // rows this launch takes: 0 all, 1 top-k/one-element rows, 2 the others
+  int exact;    // row kernel: skip the sample and the band, always select over the whole row
 };
 
 constexpr int kMaxRowList = 256;  // rows one worker (CTA or cluster) may own in a filtered launch
@@ -228,7 +231,7 @@ __device__ __forceinline__ float softmax_weight(float x, float M) {
   return __fmaf_rn(e, lo, e);
 }
 __device__ __forceinline__ unsigned long long fixed_mass(float w) {
-  return __float2ull_rn(w * kFixScale);
+  return fixed_mass_of(w);
 }
 
 // Linear bin of y in [lo, M]: min(nb - 1, floor((M - y) * s)); monotone
@@ -1516,7 +1519,7 @@ __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P)
 }
 
 
-#include "kps_stream.cuh"
+#include "kps_row.cuh"
 
 // ------------------------------------------------------------------------------------------
 // Host side
@@ -1646,18 +1649,24 @@ static kps_status choose_launch(int64_t B, int64_t V, LaunchCfg* out) {
   return KPS_OK;
 }
 
-// Kernel choice: 0 = automatic, 1 = cluster kernel only, 2 = streaming kernel where supported.
-static int g_policy = 0;
-constexpr int64_t kStreamMinRows = 64;  // automatic: the streaming kernel from this batch size up
+// The kernel the calling thread's last successful kps_sample launched (1 cluster, 2 row).
+static thread_local int t_last_kernel = 0;
 
-struct StreamCfg {
-  int stages;
+// Kernel choice: 0 = automatic, 1 = cluster kernel only, 2 = row kernel where supported,
+// 3 = row kernel with the exact whole-row selection forced (a test hook).
+static int g_policy = 0;
+constexpr int64_t kRowMinRows = 64;  // automatic: the row kernel from this batch size up
+
+constexpr int kRowTeams[] = {2, 1};  // cluster sizes tried, widest first: CTAs sharing a top-p-only row
+
+struct RowCfg {
   size_t smem;
-  int ctas;
+  int cs;        // cluster size
+  int clusters;  // clusters resident at once (the persistent grid, in clusters)
 };
 
 template <bool kBF16>
-static cudaError_t prepare_stream_kernel() {
+static cudaError_t prepare_row_kernel() {
   static std::mutex mu;
   static bool done[64] = {};
   int dev = 0;
@@ -1667,45 +1676,48 @@ static cudaError_t prepare_stream_kernel() {
   std::lock_guard<std::mutex> lock(mu);
   if (done[dev]) return cudaSuccess;
   cudaFuncAttributes fa;
-  err = cudaFuncGetAttributes(&fa, kps_stream_kernel<kBF16>);
+  err = cudaFuncGetAttributes(&fa, kps_row_kernel<kBF16>);
   if (err != cudaSuccess) return err;
   const int optin = device_smem_optin() - static_cast<int>(fa.sharedSizeBytes);
-  err = cudaFuncSetAttribute(kps_stream_kernel<kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+  err = cudaFuncSetAttribute(kps_row_kernel<kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
   if (err == cudaSuccess) done[dev] = true;
   return err;
 }
 
-// Ring depth and grid of the streaming kernel; false if it cannot run this shape.
+// Shared memory and resident grid of the row kernel; false if it cannot run this V.
 template <bool kBF16>
-static bool choose_stream(int64_t B, int64_t V, StreamCfg* out) {
-  if (V > kSMaxV) return false;
-  if (prepare_stream_kernel<kBF16>() != cudaSuccess) {
+static bool choose_row(int64_t V, RowCfg* out) {
+  if (V > kRMaxV) return false;
+  if (prepare_row_kernel<kBF16>() != cudaSuccess) {
     (void)cudaGetLastError();
     return false;
   }
-  cudaFuncAttributes fa;
-  if (cudaFuncGetAttributes(&fa, kps_stream_kernel<kBF16>) != cudaSuccess) {
-    (void)cudaGetLastError();
-    return false;
+  const size_t smem = make_rlayout(V).total;
+  for (int cs : kRowTeams) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cs);
+    cfg.blockDim = dim3(kRT);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute a[1];
+    a[0].id = cudaLaunchAttributeClusterDimension;
+    a[0].val.clusterDim.x = cs;
+    a[0].val.clusterDim.y = 1;
+    a[0].val.clusterDim.z = 1;
+    cfg.attrs = a;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kps_row_kernel<kBF16>, &cfg) != cudaSuccess) {
+      (void)cudaGetLastError();
+      n = 0;
+    }
+    if (n > 0) {
+      out->smem = smem;
+      out->cs = cs;
+      out->clusters = n;
+      return true;
+    }
   }
-  const int optin = device_smem_optin() - static_cast<int>(fa.sharedSizeBytes);
-  const SLayout base = make_slayout(V, kBF16, 0);
-  if (static_cast<size_t>(optin) <= base.total) return false;
-  int stages = static_cast<int>((static_cast<size_t>(optin) - base.total) / base.stage_bytes);
-  if (stages > kSMaxStages) stages = kSMaxStages;
-  if (stages < kSMinStages) return false;
-  const size_t smem = make_slayout(V, kBF16, stages).total;
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kps_stream_kernel<kBF16>, kSThreads, smem) != cudaSuccess ||
-      per_sm < 1) {
-    (void)cudaGetLastError();
-    return false;
-  }
-  const int64_t slots = static_cast<int64_t>(device_sm_count()) * per_sm;
-  out->stages = stages;
-  out->smem = smem;
-  out->ctas = static_cast<int>(B < slots ? B : slots);
-  return true;
+  return false;
 }
 
 // Launch decisions depend only on (device, dtype, V) plus min() with B, so they are
@@ -1714,16 +1726,15 @@ struct CachedShape {
   int dev;
   int dt;
   int64_t V;
-  bool stream_ok;
-  StreamCfg stream;
-  int64_t stream_slots;  // resident CTAs of the streaming kernel
+  bool row_ok;
+  RowCfg row;
   bool cluster_ok;
   kps_status cluster_status;
   LaunchCfg cluster;      // clusters = resident clusters (min with B at launch)
   bool cluster_small_b;   // cluster choice was made for a batch smaller than the SM count
 };
 
-static kps_status lookup_shape(kps_dtype dt, int64_t V, int64_t B, bool want_stream, CachedShape* out) {
+static kps_status lookup_shape(kps_dtype dt, int64_t V, int64_t B, CachedShape* out) {
   static std::mutex mu;
   static CachedShape cache[32];
   static int used = 0, next = 0;
@@ -1747,12 +1758,10 @@ static kps_status lookup_shape(kps_dtype dt, int64_t V, int64_t B, bool want_str
   c.dt = static_cast<int>(dt);
   c.V = V;
   c.cluster_small_b = small_b;
-  (void)want_stream;
   const int64_t bigB = 1 << 20;
-  StreamCfg sc{};
-  c.stream_ok = dt == KPS_BF16 ? choose_stream<true>(bigB, V, &sc) : choose_stream<false>(bigB, V, &sc);
-  c.stream = sc;
-  c.stream_slots = c.stream_ok ? sc.ctas : 0;
+  RowCfg rcfg{};
+  c.row_ok = dt == KPS_BF16 ? choose_row<true>(V, &rcfg) : choose_row<false>(V, &rcfg);
+  c.row = rcfg;
   LaunchCfg lc{};
   const int64_t probeB = small_b ? B : bigB;
   c.cluster_status = dt == KPS_BF16 ? choose_launch<true>(probeB, V, &lc) : choose_launch<false>(probeB, V, &lc);
@@ -1839,20 +1848,19 @@ kps_status kps_sample(const void* logits, kps_dtype dt, int64_t B, int64_t V, co
   const bool aligned = (reinterpret_cast<uintptr_t>(logits) % 16 == 0) && ((V * esize) % 16 == 0) &&
                        (reinterpret_cast<uintptr_t>(q) % 16 == 0) && (V % 4 == 0) &&
                        (!need_logits || reinterpret_cast<uintptr_t>(out_filtered) % 16 == 0);
-  const bool want_stream =
-      aligned && (kps::g_policy == 2 || (kps::g_policy == 0 && B >= kps::kStreamMinRows));
-  kps::StreamCfg scfg;
+  const bool want_row =
+      aligned && (kps::g_policy >= 2 || (kps::g_policy == 0 && B >= kps::kRowMinRows));
+  kps::RowCfg rcfg;
   kps::LaunchCfg cfg;
-  bool use_stream = false;
+  bool use_row = false;
   {
     kps::CachedShape cs;
-    const kps_status st = kps::lookup_shape(dt, V, B, want_stream, &cs);
+    const kps_status st = kps::lookup_shape(dt, V, B, &cs);
     if (st != KPS_OK) return st;
-    use_stream = want_stream && cs.stream_ok;
-    scfg = cs.stream;
-    scfg.ctas = static_cast<int>(B < cs.stream_slots ? B : cs.stream_slots);
+    use_row = want_row && cs.row_ok;
+    rcfg = cs.row;
     cfg = cs.cluster;
-    if (!use_stream && !cs.cluster_ok) return cs.cluster_status;
+    if (!use_row && !cs.cluster_ok) return cs.cluster_status;
   }
 
   kps::Params P;
@@ -1874,31 +1882,32 @@ kps_status kps_sample(const void* logits, kps_dtype dt, int64_t B, int64_t V, co
   P.nc = cfg.nc;
   P.use_tma = aligned ? 1 : 0;
   P.filter = 0;
+  P.exact = kps::g_policy == 3 ? 1 : 0;
 
-  // Automatic mode splits the batch: the streaming kernel takes the top-k and
-  // one-element rows (one HBM pass each, one SM per row), then the cluster kernel
-  // takes the rest (top-p over the whole row, or every element kept), whose
-  // per-element softmax work is spread over a cluster of SMs per row.
-  const int64_t cl_workers = B < cfg.clusters ? B : cfg.clusters;
-  const bool split = use_stream && kps::g_policy == 0 && cfg.clusters > 0 &&
-                     B <= static_cast<int64_t>(kps::kMaxRowList) * scfg.ctas &&
-                     B <= static_cast<int64_t>(kps::kMaxRowList) * cl_workers;
-  if (use_stream) {
-    cudaLaunchConfig_t sl = {};
-    sl.gridDim = dim3(static_cast<unsigned>(scfg.ctas));
-    sl.blockDim = dim3(kps::kSThreads);
-    sl.dynamicSmemBytes = scfg.smem;
-    sl.stream = stream;
-    const int stages = scfg.stages;
-    P.filter = split ? 1 : 0;
-    cudaError_t e = dt == KPS_BF16 ? cudaLaunchKernelEx(&sl, kps::kps_stream_kernel<true>, P, stages)
-                                   : cudaLaunchKernelEx(&sl, kps::kps_stream_kernel<false>, P, stages);
+  if (use_row) {
+    // a persistent grid of resident clusters; a cluster's CTAs share the top-p-only and
+    // keep-all rows and take the other rows one each
+    const int64_t ncl = B < rcfg.clusters ? B : rcfg.clusters;
+    cudaLaunchConfig_t rl = {};
+    rl.gridDim = dim3(static_cast<unsigned>(ncl * rcfg.cs));
+    rl.blockDim = dim3(kps::kRT);
+    rl.dynamicSmemBytes = rcfg.smem;
+    rl.stream = stream;
+    cudaLaunchAttribute rattr[1];
+    rattr[0].id = cudaLaunchAttributeClusterDimension;
+    rattr[0].val.clusterDim.x = rcfg.cs;
+    rattr[0].val.clusterDim.y = 1;
+    rattr[0].val.clusterDim.z = 1;
+    rl.attrs = rattr;
+    rl.numAttrs = 1;
+    cudaError_t e = dt == KPS_BF16 ? cudaLaunchKernelEx(&rl, kps::kps_row_kernel<true>, P)
+                                   : cudaLaunchKernelEx(&rl, kps::kps_row_kernel<false>, P);
     if (e != cudaSuccess) {
       (void)cudaGetLastError();
       return KPS_ERR_CUDA;
     }
-    if (!split) return KPS_OK;
-    P.filter = 2;
+    kps::t_last_kernel = 2;
+    return KPS_OK;
   }
 
   cudaLaunchConfig_t lc = {};
@@ -1920,16 +1929,19 @@ kps_status kps_sample(const void* logits, kps_dtype dt, int64_t B, int64_t V, co
     (void)cudaGetLastError();
     return KPS_ERR_CUDA;
   }
+  kps::t_last_kernel = 1;
   return KPS_OK;
 }
 
 kps_status kps_set_kernel_policy(int policy) {
-  if (policy < 0 || policy > 2) return KPS_ERR_INVALID_ARG;
+  if (policy < 0 || policy > 3) return KPS_ERR_INVALID_ARG;
   kps::g_policy = policy;
   return KPS_OK;
 }
 
 int kps_get_kernel_policy(void) { return kps::g_policy; }
+
+int kps_last_kernel(void) { return kps::t_last_kernel; }
 
 kps_status kps_last_device_status(void* workspace, cudaStream_t stream, int* out) {
   if (!workspace || !out) return KPS_ERR_INVALID_ARG;

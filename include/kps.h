@@ -144,17 +144,25 @@ kps_status kps_sample_noalloc(const void* logits, kps_dtype dt, int64_t B, int64
                               int64_t* out_idx, float* out_filtered, cudaStream_t stream);
 
 /* Kernel selection, process-wide (for tests and tuning):
- *   0 = automatic (default): the streaming kernel — one CTA per row at a
- *       time, each row streamed once through a TMA ring — for batches of at
- *       least 64 rows whose rows are 16-byte aligned and V <= 262144; the
- *       cluster kernel — one thread-block cluster per row, the row resident
- *       in the cluster's shared memory — otherwise;
+ *   0 = automatic (default): the row kernel — one CTA per row, the row read
+ *       from global memory with 16-byte loads, two CTAs per SM — for batches
+ *       of at least 64 rows whose rows are 16-byte aligned and V <= 262144;
+ *       the cluster kernel — one thread-block cluster per row, the row
+ *       resident in the cluster's shared memory — otherwise;
  *   1 = always the cluster kernel;
- *   2 = the streaming kernel whenever the shape allows it.
+ *   2 = the row kernel whenever the shape allows it;
+ *   3 = as 2, with the row kernel's exact whole-row selection forced on
+ *       every row (the path it takes when its sample misses); slow, for
+ *       tests of that path.
  * Both compute the same results.  Not thread-safe against concurrent
  * kps_sample calls. */
 kps_status kps_set_kernel_policy(int policy);
 int kps_get_kernel_policy(void);
+
+/* Which kernel the most recent kps_sample call of the calling host thread
+ * that launched one used: 1 = the cluster kernel (kps_sample_kernel),
+ * 2 = the row kernel (kps_row_kernel), 0 = none yet. */
+int kps_last_kernel(void);
 
 /* Static description of a status code. */
 const char* kps_status_string(kps_status s);

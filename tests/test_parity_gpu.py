@@ -28,14 +28,15 @@ def _built():
     oracle.build()
 
 
-@pytest.fixture(params=["cluster", "stream", "auto"])
+@pytest.fixture(params=["cluster", "row", "row_exact", "auto"])
 def kernel(request):
-    """Runs the test under each kernel policy: the cluster kernel alone, the streaming
-    kernel alone (it only takes aligned rows; other shapes fall back to the cluster
-    kernel), and the automatic split of one batch between the two."""
+    """Runs the test under each kernel policy: the cluster kernel alone, the row kernel
+    alone (it only takes aligned rows; other shapes fall back to the cluster kernel),
+    the row kernel with its exact whole-row selection forced on every row (the path a
+    missed sample or an overflowing band takes), and the automatic choice by batch size."""
     import decode_token_sampling_gb300 as kps
-    kps.set_kernel_policy({"cluster": kps.KERNEL_CLUSTER, "stream": kps.KERNEL_STREAM,
-                           "auto": kps.KERNEL_AUTO}[request.param])
+    kps.set_kernel_policy({"cluster": kps.KERNEL_CLUSTER, "row": kps.KERNEL_ROW,
+                           "row_exact": kps.KERNEL_ROW_EXACT, "auto": kps.KERNEL_AUTO}[request.param])
     yield request.param
     kps.set_kernel_policy(kps.KERNEL_AUTO)
 
@@ -69,10 +70,11 @@ def test_ties_and_specials(V, kernel):
     compare(inp, ref, gi, gf, f"ties V={V}")
 
 
-def test_all_equal_rows_split_ties_by_index(kernel):
-    inp = make_random(8, 3000, seed=11)
+@pytest.mark.parametrize("V", [3000, 20000])
+def test_all_equal_rows_split_ties_by_index(V, kernel):
+    inp = make_random(8, V, seed=11)
     inp.logits[:] = 0.5
-    inp.top_k[:] = [1, 2, 17, 1024, 0, 0, 700, 3000][:8]
+    inp.top_k[:] = [1, 2, 17, 1024, 0, 0, 700, V][:8]
     inp.top_p[:] = [1.0, 0.5, 1.0, 0.25, 0.5, 0.125, 0.99, 1.0]
     inp.temperature[:] = 1.0
     ref = oracle.sample(inp)
@@ -80,8 +82,9 @@ def test_all_equal_rows_split_ties_by_index(kernel):
     compare(inp, ref, gi, gf, "all-equal")
 
 
-def test_edge_parameters(kernel):
-    B, V = 16, 3001
+@pytest.mark.parametrize("V", [3001, 3000, 12288])
+def test_edge_parameters(V, kernel):
+    B = 16
     inp = make_random(B, V, seed=99, penalty=1.2, n_seen=40)
     inp.top_k[:] = [0, -1, 1, 1024, 1025, V, V + 7, 5, 50, 1, 0, 3, 2, 1000, 7, 9]
     inp.top_p[:] = [0.0, -1.0, np.nan, 1.0, 1.5, 1e-7, 0.999999, 0.5, 0.9, 0.3, 0.95, 0.0, 1.0, 0.7, np.nan, 0.8]
@@ -89,11 +92,12 @@ def test_edge_parameters(kernel):
     inp.penalty[:] = [1.2, 0.0, -1.0, np.nan, 1.0, 1.2, 1.2, 2.0, 0.5, 1.2, 1.2, 1.2, 1.2, 1.2, 1.2, 1.2]
     ref = oracle.sample(inp)
     gi, gf = run_gpu(inp)
-    compare(inp, ref, gi, gf, "edge params")
+    compare(inp, ref, gi, gf, f"edge params V={V}")
 
 
-def test_q_edge_values(kernel):
-    inp = make_random(6, 2048, seed=5)
+@pytest.mark.parametrize("V", [2048, 10240])
+def test_q_edge_values(V, kernel):
+    inp = make_random(6, V, seed=5)
     inp.q[0, :] = 0.0
     inp.q[1, ::2] = np.inf
     inp.q[2, :] = 1.0
@@ -101,7 +105,7 @@ def test_q_edge_values(kernel):
     inp.q[4, :] = 1e-30
     ref = oracle.sample(inp)
     gi, gf = run_gpu(inp)
-    compare(inp, ref, gi, gf, "q edges")
+    compare(inp, ref, gi, gf, f"q edges V={V}")
 
 
 def test_zero_rows_is_noop():
