@@ -42,11 +42,7 @@ constexpr int kRMaxV = 262144;          // the row's penalty bitmap lives in sha
 constexpr int kRRuns = 64;              // sampled runs of 32 consecutive elements
 constexpr int kRSamp = kRRuns * 32;
 constexpr int kRLin = 2048;             // linear count bins of the buffer selection
-constexpr int kRMassBins = 4096;        // approximate mass bins of top-p-only rows
-constexpr float kRBinScale = 64.0f;     // ... per unit of H - y
-constexpr float kRHeadroom = 16.0f;     // H = sample maximum + headroom
-constexpr float kRMassUnit = 8192.0f;   // approximate weight inside a bin, in units of 2^-13
-constexpr double kRBandMargin = 1e-4;   // relative error allowed to the approximate prefix mass
+constexpr float kRHeadroom = 16.0f;     // top-p-only rows: H = sample maximum + headroom
 constexpr int kRSurvBins = 1024;        // linear mass bins of top-p over the survivors
 constexpr int kRHistWords = 6144;
 constexpr int kRRank = 256;             // boundary-bin entries ranked pairwise
@@ -123,20 +119,33 @@ __device__ __forceinline__ void unpack16(const uint4 w, float* v) {
   }
 }
 
+// 1/x to about one ulp (the hardware approximation): race quotients only decide near-ties
+// differently from the exact ones.
+__device__ __forceinline__ float rrcp_approx(float x) {
+  float r;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
 // Shared-memory add without a return value (the pointer must address shared memory).
 __device__ __forceinline__ void sh_red_add(uint32_t* p, uint32_t v) {
   asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
 }
 
+// Out-of-line IEEE division: the rare paths call it, so the common path never pays for
+// (or speculates) the full division sequence.
+__device__ __noinline__ float rdiv_ieee(float x, float d) { return __fdiv_rn(x, d); }
+
 // Penalty of a seen element (applied after NaN -> -inf).
 __device__ __forceinline__ float rpenal(float x, float pen) {
-  return (x > 0.0f) ? __fdiv_rn(x, pen) : __fmul_rn(x, pen);
+  return (x > 0.0f) ? rdiv_ieee(x, pen) : __fmul_rn(x, pen);
 }
 // x / T rounded to nearest: the multiply-and-correct quotient inside its safe range, the
 // IEEE division outside it.
 __device__ __forceinline__ float rdiv(float x, const FixedDivisor& dv) {
   const float q = div_fast(x, dv);
-  return (dv.fast && div_ok(x, q)) ? q : __fdiv_rn(x, dv.T);
+  if (dv.fast && div_ok(x, q)) return q;
+  return rdiv_ieee(x, dv.T);
 }
 // Transformed value: NaN -> -inf, the penalty if the element was seen, x / T
 // (unless the row is greedy), -0 -> +0.
@@ -1220,23 +1229,56 @@ __device__ __noinline__ int32_t rrow_first_max(const RowCtx& rc, float M, unsign
   return static_cast<int32_t>(~static_cast<uint32_t>(best));
 }
 
-// Approximate-mass bin of y below the reference H (>= every y of the row): width 1/64,
-// kRMassBins when y lies 64 or more below H (then it carries no fixed-point mass).
-__device__ __forceinline__ int rmass_bin(float y, float H) {
-  if (y == H) return 0;
-  const float d = __fsub_rn(H, y);
-  if (!(d < 64.0f)) return kRMassBins;
-  return rfloor_small(__fmul_rn(d, kRBinScale));
+// ---- top-p-only rows: pass A (histogram), pass B (race, write, band) -------------------
+
+constexpr int kRPBins = 2048;           // mass bins of top-p-only rows: width 1/32 below H
+constexpr float kRPScale = 32.0f;
+
+// The weight of y against a reference H >= y: its bin b = floor(32 (H - y)) (kRPBins when
+// H - y >= 64, or y > H: no mass) and exp(-(H - y - b/32)), the weight relative to the bin
+// top, as an integer in units of 2^-24 (the difference H - y is carried exactly, so the
+// only error is the exponential's, about 2^-22 relative).  The mass of an element is
+// w24 * 2^-24 * exp(-b/32) against exp(H); every total, prefix and race below is taken in
+// this one arithmetic, so they agree with each other exactly.
+struct PW {
+  int b;
+  uint32_t w24;
+  float frac;  // H - y - b/32, in [0, 1/32) up to rounding: the position inside the bin
+};
+__device__ __forceinline__ PW pweight(float y, float H) {
+  // branch-free: every element of a warp takes the same instructions
+  const bool top = y == H;  // also covers +-inf maxima
+  const float d = top ? 0.0f : __fsub_rn(H, y);
+  const bool valid = d >= 0.0f && d < 64.0f;  // false for NaN and for y > H
+  const float bb = __fsub_rn(d, H);
+  const float dl0 = __fadd_rn(__fsub_rn(H, __fsub_rn(d, bb)), __fsub_rn(-y, bb));  // H - y = d + dl
+  const float dl = top ? 0.0f : dl0;
+  const float f = __fmul_rn(valid ? d : 0.0f, kRPScale);
+  const float t = __fadd_rd(f, 8388608.0f);  // floor(f) + 2^23
+  const int b = __float_as_int(t) - 0x4B000000;
+  const float frac = __fadd_rn(__fmul_rn(__fsub_rn(f, __fsub_rn(t, 8388608.0f)), 1.0f / kRPScale), dl);
+  const float v = __fmul_rn(__expf(-(valid ? frac : 0.0f)), 16777216.0f);  // an integer in [2^23, 2^24 + 2]
+  const uint32_t u = __float_as_uint(v);
+  PW r;
+  r.b = valid ? b : kRPBins;
+  r.w24 = valid ? ((u & 0x7FFFFFu) | 0x800000u) << ((u >> 23) - 150u) : 0u;
+  r.frac = valid ? frac : 0.0f;
+  return r;
 }
 
-// Pass A of top-p-only rows over this CTA's part: the approximate mass histogram against
-// H (y taken as x * (1/T), which may differ from x / T in the last bit: the histogram
-// only has to be close, and pass B re-bins with the exact quotient).  Returns the part's
-// largest penalised raw value as a key.
-constexpr int kRUA = 8;  // loads in flight per thread in pass A
+constexpr int kRPSub = 1024;  // sub-bins of the boundary bin (by position inside it)
+
+// Sub-bin of an element of the boundary bin: non-decreasing in H - y.
+__device__ __forceinline__ int psub(const PW& w) {
+  return rfloor_small(fminf(fmaxf(__fmul_rn(w.frac, kRPScale * kRPSub), 0.0f), static_cast<float>(kRPSub - 1)));
+}
+
+// Pass A of top-p-only rows over this CTA's part: the exact transformed values, binned
+// against H with their 24-bit weights summed per bin in two 12/13-bit limbs
+// (h[b], h[kRPBins + b]: a bin takes any row of at most 2^18 elements without overflow).
+// Returns the part's largest value as a key.
 template <bool kBF16>
-__device__ __noinline__ unsigned long long rp_pass_a(const RowCtx& rc, float H, uint32_t* h,
-                                                     unsigned long long* red) {
+__device__ __noinline__ unsigned long long rp_pass_a(const RowCtx& rc, float H, uint32_t* h, unsigned long long* red) {
   constexpr int G = kBF16 ? 8 : 4;
   const unsigned long long pol = l2_policy_last();
   const uint4* xr = rc.x;
@@ -1244,24 +1286,26 @@ __device__ __noinline__ unsigned long long rp_pass_a(const RowCtx& rc, float H, 
   const uint32_t* bitmap = rc.bitmap;
   const bool pen_on = rc.pen_on, identity = rc.identity;
   const float pen = rc.pen;
-  const float invT = identity ? 1.0f : __frcp_rn(rc.T);
-  for (int i = threadIdx.x; i < kRMassBins; i += kRT) h[i] = 0u;
+  const FixedDivisor dv = rc.div;
+  for (int i = threadIdx.x; i < 2 * kRPBins; i += kRT) h[i] = 0u;
   __syncthreads();
-  float xm = -INFINITY;
-  for (int base = g0; base < g1; base += kRT * kRUA) {
-    uint4 w[kRUA];
+  unsigned long long kmax = 0;
+  for (int base = g0; base < g1; base += kRT * kRU) {
+    uint4 w[kRU];
 #pragma unroll
-    for (int u = 0; u < kRUA; ++u) {
+    for (int u = 0; u < kRU; ++u) {
       const int g = base + u * kRT + static_cast<int>(threadIdx.x);
       w[u] = g < g1 ? ld_row16(xr + g, pol) : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
-    for (int u = 0; u < kRUA; ++u) {
+    for (int u = 0; u < kRU; ++u) {
       const int g = base + u * kRT + static_cast<int>(threadIdx.x);
       if (g >= g1) continue;
       float v[G];
       unpack16<kBF16>(w[u], v);
       const uint32_t bits = rseen_bits<G>(bitmap, pen_on, g);
+#pragma unroll
+      for (int e = 0; e < G; ++e) v[e] = isnan(v[e]) ? -INFINITY : v[e];
       if (bits) {
 #pragma unroll
         for (int e = 0; e < G; ++e)
@@ -1269,34 +1313,30 @@ __device__ __noinline__ unsigned long long rp_pass_a(const RowCtx& rc, float H, 
       }
 #pragma unroll
       for (int e = 0; e < G; ++e) {
-        xm = fmaxf(xm, v[e]);  // NaN is ignored (it counts as -inf)
-        const float y = __fmul_rn(v[e], invT);
-        const float d = y == H ? 0.0f : __fsub_rn(H, y);  // +-inf maxima equal to H fall in bin 0
-        if (d < 64.0f) {                                  // false for NaN, and for -inf
-          const float f = __fmul_rn(fmaxf(d, 0.0f), kRBinScale);
-          const float t = __fadd_rd(f, 8388608.0f);  // floor(f) + 2^23
-          const int b = __float_as_int(t) - 0x4B000000;
-          const float frac = __fsub_rn(f, __fsub_rn(t, 8388608.0f));
-          const float wr = __fmul_rn(__expf(-frac * (1.0f / kRBinScale)), kRMassUnit);
-          sh_red_add(&h[b], static_cast<uint32_t>(__float_as_int(__fadd_rn(wr, 8388608.0f)) - 0x4B000000));
+        const float y = __fadd_rn(identity ? v[e] : rdiv(v[e], dv), 0.0f);
+        const unsigned long long ky = fkey(y);
+        kmax = ky > kmax ? ky : kmax;
+        const PW pw = pweight(y, H);
+        if (pw.b < kRPBins) {
+          sh_red_add(&h[pw.b], pw.w24 & 0xFFFu);
+          sh_red_add(&h[kRPBins + pw.b], pw.w24 >> 12);
         }
       }
     }
   }
-  unsigned long long k = fkey(xm), dummy = 0;
-  rblock_max2(k, dummy, red);
-  return k;
+  unsigned long long dummy = 0;
+  rblock_max2(kmax, dummy, red);
+  return kmax;
 }
 
-// Pass B of top-p-only rows over this CTA's part: the exact fixed-point mass of the part
-// (*S), of the elements above the band (*above; kept: raced and written), and the band
-// appended to the warps' segments of cw.  *rb, *first: per-thread race results.
+// Pass B of top-p-only rows over this CTA's part: every element in a bin above bstar is
+// kept (raced with its weight from pass A's arithmetic, written); bin bstar goes to the
+// warps' segments of cw; the rest is written as -inf.  ftab[b] = exp(-b/32).  *rb: the
+// block's best race word.
 constexpr int kRUB = 2;  // loads in flight per thread in pass B (its registers go to the arithmetic)
 template <bool kBF16>
-__device__ __noinline__ void rp_pass_b(const RowCtx& rc, float H, float M, int blo, int bhi, float eps,
-                                       unsigned long long* cw, unsigned long long* S_out,
-                                       unsigned long long* above_out, unsigned long long* rb_out,
-                                       unsigned long long* first_out, uint32_t* wcnt_out) {
+__device__ __noinline__ void rp_pass_b(const RowCtx& rc, float H, int bstar, const float* ftab, float eps,
+                                       unsigned long long* cw, unsigned long long* rb_out, uint32_t* wcnt_out) {
   constexpr int G = kBF16 ? 8 : 4;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const unsigned lt = (1u << lane) - 1u;
@@ -1310,7 +1350,6 @@ __device__ __noinline__ void rp_pass_b(const RowCtx& rc, float H, float M, int b
   const bool pen_on = rc.pen_on, identity = rc.identity;
   const float pen = rc.pen;
   const FixedDivisor dv = rc.div;
-  unsigned long long Spart = 0, above = 0;
   float rbest = -1.0f;  // best race quotient so far and its index (ties: lower index)
   int ridx = INT_MAX;
   uint32_t wcnt = 0;
@@ -1343,26 +1382,21 @@ __device__ __noinline__ void rp_pass_b(const RowCtx& rc, float H, float M, int b
 #pragma unroll
       for (int e = 0; e < G; ++e) {
         v[e] = __fadd_rn(identity ? v[e] : rdiv(v[e], dv), 0.0f);
-        const int b = in ? rmass_bin(v[e], H) : kRMassBins + 1;
-        kmask |= (b < blo ? 1u : 0u) << e;
-        bmask |= (b >= blo && b <= bhi ? 1u : 0u) << e;
-        if (b < kRMassBins) {
-          const float wt = softmax_weight(v[e], M);
-          const unsigned long long fm = fixed_mass(wt);
-          Spart += fm;
-          if (b < blo) {
-            above += fm;
-            const int idx = g * G + e;
-            // the race quotient to about one ulp: only near-ties can change
-            const float4 q4 = qv[u][e / 4];
-            const float qe = (e & 3) == 0 ? q4.x : (e & 3) == 1 ? q4.y : (e & 3) == 2 ? q4.z : q4.w;
-            const float r = __fmul_rn(wt, __fdividef(1.0f, __fadd_rn(qe, eps)));
-            if (r > rbest || (r == rbest && idx < ridx)) {  // false for NaN
-              rbest = r;
-              ridx = idx;
-            }
-          }
-        }
+        const PW pw = pweight(v[e], H);
+        const bool kept = in && pw.b < bstar;
+        kmask |= (kept ? 1u : 0u) << e;
+        bmask |= (in && pw.b == bstar ? 1u : 0u) << e;
+        // the race, branch-free: the quotient to about one ulp (only near-ties can change);
+        // a thread meets its elements in increasing index order, so a strict > keeps the
+        // lower index
+        const float wt = __fmul_rn(__fmul_rn(static_cast<float>(pw.w24), 5.9604644775390625e-8f),
+                                   ftab[pw.b < kRPBins ? pw.b : kRPBins - 1]);
+        const float4 q4 = qv[u][e / 4];
+        const float qe = (e & 3) == 0 ? q4.x : (e & 3) == 1 ? q4.y : (e & 3) == 2 ? q4.z : q4.w;
+        const float r = __fmul_rn(wt, rrcp_approx(__fadd_rn(qe, eps)));
+        const bool better = kept && r > rbest;  // false for NaN
+        rbest = better ? r : rbest;
+        ridx = better ? g * G + e : ridx;
       }
       if (__any_sync(kFull, bmask != 0u)) {
 #pragma unroll
@@ -1388,10 +1422,7 @@ __device__ __noinline__ void rp_pass_b(const RowCtx& rc, float H, float M, int b
       }
     }
   }
-  *S_out = Spart;
-  *above_out = above;
   *rb_out = rbest >= 0.0f ? order_word(fkey(rbest), ridx) : 0ull;
-  *first_out = 0ull;  // the first kept element is the row's first maximum: found when needed
   *wcnt_out = wcnt;
 }
 
@@ -1451,59 +1482,83 @@ __device__ __noinline__ int32_t rwide_row(const RowCtx& rc, const RowSmem& sm, c
     tm.sync();
     H = rmax_transformed(tm.max_of(sm.misc, 0), rc);
   }
-  // pass A; again with H = M when the sample missed the top of the row
+  // pass A; again with H = M when the sample missed the top of the row by more than the headroom
   tm.push(sm.misc, 1, rp_pass_a<kBF16>(rc, H, sm.hist, sm.red));
   tm.sync();
-  float M = rmax_transformed(tm.max_of(sm.misc, 1), rc);
+  const float M = kfloat(static_cast<uint32_t>(tm.max_of(sm.misc, 1)));
   if (M > H) {
     H = M;
-    tm.sync();  // every member has read slot 1
+    tm.sync();  // every member has read slot 1 and is done with the sample
     tm.push(sm.misc, 1, rp_pass_a<kBF16>(rc, H, sm.hist, sm.red));
     tm.sync();
   }
-  // the band: bins whose approximate prefix mass (summed over the members) is within
-  // the margin of p * S
+  // bin factors exp(-b/32), the bin masses summed over the members, their total S, and
+  // the bin bstar holding the boundary (its prefix reaches p * S)
+  float* ftab = reinterpret_cast<float*>(sm.wbuf);
+  for (int b = threadIdx.x; b < kRPBins; b += kRT) ftab[b] = __expf(-static_cast<float>(b) * (1.0f / kRPScale));
+  double above = 0.0, tq = 0.0;
+  int bstar;
   {
-    constexpr int per = kRMassBins / kRT;
-    unsigned long long m[per];
-    unsigned long long sum = 0;
+    constexpr int per = kRPBins / kRT;
+    double m[per];
+    double sum = 0.0;
 #pragma unroll
     for (int e = 0; e < per; ++e) {
       const int b = per * static_cast<int>(threadIdx.x) + e;
-      uint32_t cnt = 0;
-      for (int r = 0; r < tm.C; ++r) cnt += tm.remote(sm.hist, r)[b];
-      // bin mass in units of 2^-40 of exp(y - H): count * 2^-13 * exp(-b/64) * 2^40
-      m[e] = static_cast<unsigned long long>(static_cast<float>(cnt) *
-                                             __expf(-static_cast<float>(b) * (1.0f / kRBinScale)) * 134217728.0f);
+      unsigned long long c = 0;
+      for (int r = 0; r < tm.C; ++r) {
+        const uint32_t* hr = tm.remote(sm.hist, r);
+        c += static_cast<unsigned long long>(hr[b]) + (static_cast<unsigned long long>(hr[kRPBins + b]) << 12);
+      }
+      m[e] = static_cast<double>(c) * 5.9604644775390625e-8 *
+             static_cast<double>(__expf(-static_cast<float>(b) * (1.0f / kRPScale)));
       sum += m[e];
     }
-    if (threadIdx.x == 0) {
-      sm.misc[kMBlo] = 0ull;
-      sm.misc[kMBhi] = static_cast<unsigned long long>(kRMassBins - 1);
+    if (threadIdx.x == 0) sm.misc[kMBin] = static_cast<unsigned long long>(kRPBins);
+    const int lane2 = threadIdx.x & 31, warp2 = threadIdx.x >> 5;
+    double x = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const double y = __shfl_up_sync(kFull, x, o);
+      if (lane2 >= o) x += y;
     }
-    unsigned long long Sa;
-    const unsigned long long ex = rblock_excl_scan_u64(sum, &Sa, sm.red);
-    const double t = static_cast<double>(p) * static_cast<double>(Sa);
-    const unsigned long long lo_t = static_cast<unsigned long long>(fmax(t - kRBandMargin * static_cast<double>(Sa), 0.0));
-    const unsigned long long hi_t = static_cast<unsigned long long>(t + kRBandMargin * static_cast<double>(Sa)) + 1ull;
-    unsigned long long acc = ex;
+    double* redd = reinterpret_cast<double*>(sm.red);
+    if (lane2 == 31) redd[warp2] = x;
+    __syncthreads();
+    if (warp2 == 0) {
+      const double sv = lane2 < kRW ? redd[lane2] : 0.0;
+      double t = sv;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const double y = __shfl_up_sync(kFull, t, o);
+        if (lane2 >= o) t += y;
+      }
+      if (lane2 < kRW) redd[kRW + lane2] = t - sv;
+      if (lane2 == kRW - 1) redd[48] = t;
+    }
+    __syncthreads();
+    const double S = redd[48];
+    tq = static_cast<double>(p) * S;
+    double acc = redd[kRW + warp2] + x - sum;
 #pragma unroll
     for (int e = 0; e < per; ++e) {
       const int b = per * static_cast<int>(threadIdx.x) + e;
-      const unsigned long long after = acc + m[e];
-      if (acc < lo_t && after >= lo_t) sm.misc[kMBlo] = static_cast<unsigned long long>(b);
-      if (acc < hi_t && after >= hi_t) sm.misc[kMBhi] = static_cast<unsigned long long>(b);
+      const double after = acc + m[e];
+      if (acc < tq && after >= tq) {
+        sm.misc[kMBin] = static_cast<unsigned long long>(b);
+        reinterpret_cast<double*>(sm.misc)[kMAbove] = acc;
+      }
       acc = after;
     }
-    tm.sync();  // band found; every member is done reading the histograms
+    tm.sync();  // every member is done reading the histograms and the slots
+    bstar = static_cast<int>(sm.misc[kMBin]);
+    above = reinterpret_cast<const double*>(sm.misc)[kMAbove];
   }
-  const int blo = static_cast<int>(sm.misc[kMBlo]);
-  const int bhi = static_cast<int>(sm.misc[kMBhi]);
 
   // pass B over this CTA's part
-  unsigned long long Spart, above, rb = 0, first = 0;
+  unsigned long long rb;
   uint32_t wcnt;
-  rp_pass_b<kBF16>(rc, H, M, blo, bhi, eps, sm.cw, &Spart, &above, &rb, &first, &wcnt);
+  rp_pass_b<kBF16>(rc, H, bstar, ftab, eps, sm.cw, &rb, &wcnt);
   if (lane == 0) segcnt[warp] = wcnt;
   __syncthreads();
   bool over = false;
@@ -1513,22 +1568,15 @@ __device__ __noinline__ int32_t rwide_row(const RowCtx& rc, const RowSmem& sm, c
     const int w = i / kRSeg;
     if (i - w * kRSeg >= static_cast<int>(segcnt[w])) sm.cw[i] = 0ull;
   }
-  rblock_sum_max2(Spart, rb, first, sm.red);
-  above = rblock_sum_u64(above, sm.red);
+  unsigned long long first = 0;
+  rblock_max2(rb, first, sm.red);
   const int nb = over ? kRCap + 1 : rcompact_nonzero(sm.cw, sm.red);
-  tm.push(sm.misc, 2, Spart);
-  tm.push(sm.misc, 3, above);
   tm.push(sm.misc, 4, rb);
-  tm.push(sm.misc, 5, first);
   tm.push(sm.misc, 6, static_cast<unsigned long long>(nb));
   tm.sync();
-  const unsigned long long S = tm.sum_of(sm.misc, 2);
-  const unsigned long long tq = rtopp_target(p, S);
-  above = tm.sum_of(sm.misc, 3);
   rb = tm.max_of(sm.misc, 4);
-  first = tm.max_of(sm.misc, 5);
   int total = 0;
-  bool fits = true;
+  bool fits = bstar < kRPBins;
   for (int r = 0; r < tm.C; ++r) {
     const int n = static_cast<int>(tm.get(sm.misc, 6, r));
     fits = fits && n <= kRCap;
@@ -1547,25 +1595,200 @@ __device__ __noinline__ int32_t rwide_row(const RowCtx& rc, const RowSmem& sm, c
   }
   tm.sync();  // the band is gathered; the other members may reuse their buffers
   if (tm.rank != 0) return -1;
-  int L = 0;
+  // the boundary inside bin bstar: a histogram of the band's exact weights over 1024
+  // sub-bins (by position in the bin) finds the sub-bin holding it, whose few entries are
+  // ranked pairwise; a crowded sub-bin sorts the whole band instead
+  const float fbf = ftab[bstar];
+  const double fb = static_cast<double>(fbf) * 5.9604644775390625e-8;
+  int L = 0;           // > 0: the sorted band's kept prefix (sort path)
+  bool have_th = false;
+  Thresh bth{0u, -1};  // the boundary entry (sub-bin path)
   if (fits) {
-    int N = 1;
-    while (N < total) N <<= 1;
-    rbitonic_desc(sm.cw, N);
-    L = rlist_topp_cut(sm.cw, total, M, above, tq, sm.red, sm.misc);
+    uint32_t* sh = sm.hist;  // kRPSub words of low limbs, then kRPSub of high limbs
+    for (int i = threadIdx.x; i < 2 * kRPSub; i += kRT) sh[i] = 0u;
+    uint32_t& s_cnt = *reinterpret_cast<uint32_t*>(sm.misc + kMCnt);
+    if (threadIdx.x == 0) {
+      sm.misc[kMBin] = ~0ull;
+      sm.misc[kMHit] = 0ull;
+      s_cnt = 0u;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < total; i += kRT) {
+      const PW w = pweight(kfloat(static_cast<uint32_t>(sm.cw[i] >> 32)), H);
+      const int sb = psub(w);
+      sh_red_add(&sh[sb], w.w24 & 0xFFFu);
+      sh_red_add(&sh[kRPSub + sb], w.w24 >> 12);
+    }
+    __syncthreads();
+    constexpr int per = kRPSub / kRT;
+    double m[per];
+    double sum = 0.0;
+#pragma unroll
+    for (int e = 0; e < per; ++e) {
+      const int b = per * static_cast<int>(threadIdx.x) + e;
+      m[e] = static_cast<double>(static_cast<unsigned long long>(sh[b]) +
+                                 (static_cast<unsigned long long>(sh[kRPSub + b]) << 12)) * fb;
+      sum += m[e];
+    }
+    const int lane2 = threadIdx.x & 31, warp2 = threadIdx.x >> 5;
+    double x = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const double y = __shfl_up_sync(kFull, x, o);
+      if (lane2 >= o) x += y;
+    }
+    double* redd = reinterpret_cast<double*>(sm.red);
+    if (lane2 == 31) redd[warp2] = x;
+    __syncthreads();
+    if (warp2 == 0) {
+      const double sv = lane2 < kRW ? redd[lane2] : 0.0;
+      double t = sv;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const double y = __shfl_up_sync(kFull, t, o);
+        if (lane2 >= o) t += y;
+      }
+      if (lane2 < kRW) redd[kRW + lane2] = t - sv;
+    }
+    __syncthreads();
+    double acc = above + redd[kRW + warp2] + x - sum;
+    if (above < tq) {
+#pragma unroll
+      for (int e = 0; e < per; ++e) {
+        const int b = per * static_cast<int>(threadIdx.x) + e;
+        if (acc < tq && acc + m[e] >= tq) {
+          sm.misc[kMBin] = static_cast<unsigned long long>(b);
+          reinterpret_cast<double*>(sm.misc)[kMAbove] = acc;
+        }
+        acc += m[e];
+      }
+    }
+    __syncthreads();
+    const unsigned long long beta = sm.misc[kMBin];
+    const double before = reinterpret_cast<const double*>(sm.misc)[kMAbove];
+    if (beta != ~0ull) {
+      // the entries of sub-bin beta, with their weights
+      unsigned long long* gw = sm.wbuf;  // order words
+      double* gm = reinterpret_cast<double*>(sm.wbuf + kRRank);
+      for (int i = threadIdx.x; i < total; i += kRT) {
+        const unsigned long long wd = sm.cw[i];
+        const PW w = pweight(kfloat(static_cast<uint32_t>(wd >> 32)), H);
+        if (psub(w) == static_cast<int>(beta)) {
+          const uint32_t pos = atomicAdd(&s_cnt, 1u);
+          if (pos < static_cast<uint32_t>(kRRank)) {
+            gw[pos] = wd;
+            gm[pos] = static_cast<double>(w.w24) * fb;
+          }
+        }
+      }
+      __syncthreads();
+      const int mcount = static_cast<int>(s_cnt);
+      if (mcount <= kRRank) {
+        for (int i = threadIdx.x; i < mcount; i += kRT) {
+          const unsigned long long wi = gw[i];
+          double ex = before;
+          for (int j = 0; j < mcount; ++j) ex += gw[j] > wi ? gm[j] : 0.0;
+          if (ex < tq && tq <= ex + gm[i]) sm.misc[kMHit] = wi;
+        }
+      }
+      __syncthreads();
+      const unsigned long long hit = sm.misc[kMHit];
+      if (hit) {
+        have_th = true;
+        bth = Thresh{static_cast<uint32_t>(hit >> 32), static_cast<int32_t>(~static_cast<uint32_t>(hit))};
+      }
+      __syncthreads();
+    }
+    if (!have_th) {
+      // crowded sub-bin: sort the band and cut the first entry whose prefix reaches tq
+      int N = 1;
+      while (N < total) N <<= 1;
+      rbitonic_desc(sm.cw, N);
+      constexpr int per2 = kRSortMax / kRT;
+      double wv[per2];
+      double sum2 = 0.0;
+#pragma unroll
+      for (int e = 0; e < per2; ++e) {
+        const int i = per2 * static_cast<int>(threadIdx.x) + e;
+        wv[e] = i < total ? static_cast<double>(pweight(kfloat(static_cast<uint32_t>(sm.cw[i] >> 32)), H).w24) * fb : 0.0;
+        sum2 += wv[e];
+      }
+      if (threadIdx.x == 0) sm.misc[kMCut] = 0ull;
+      double x2 = sum2;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const double y = __shfl_up_sync(kFull, x2, o);
+        if (lane2 >= o) x2 += y;
+      }
+      if (lane2 == 31) redd[warp2] = x2;
+      __syncthreads();
+      if (warp2 == 0) {
+        const double sv = lane2 < kRW ? redd[lane2] : 0.0;
+        double t = sv;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const double y = __shfl_up_sync(kFull, t, o);
+          if (lane2 >= o) t += y;
+        }
+        if (lane2 < kRW) redd[kRW + lane2] = t - sv;
+      }
+      __syncthreads();
+      double acc2 = above + redd[kRW + warp2] + x2 - sum2;
+      if (above < tq) {
+#pragma unroll
+        for (int e = 0; e < per2; ++e) {
+          const int i = per2 * static_cast<int>(threadIdx.x) + e;
+          if (i < total && acc2 < tq && acc2 + wv[e] >= tq) sm.misc[kMCut] = static_cast<unsigned long long>(i + 1);
+          acc2 += wv[e];
+        }
+      }
+      __syncthreads();
+      L = static_cast<int>(sm.misc[kMCut]);
+      __syncthreads();
+      if (L > 0) {
+        have_th = true;
+        const unsigned long long wl = sm.cw[L - 1];
+        bth = Thresh{static_cast<uint32_t>(wl >> 32), static_cast<int32_t>(~static_cast<uint32_t>(wl))};
+      }
+    }
   }
-  if (L == 0) {
-    // the band overflowed or missed the boundary: exact select over the whole row, then
-    // race and write all of it again
-    const Thresh th = rrow_select<kBF16, true>(whole, tq, M, sm.hist, sm.red, sm.misc);
+  if (!have_th) {
+    // the band overflowed or missed the boundary: the exact selection over the whole row
+    // (fixed-point masses against the true maximum), then race and write all of it again
+    unsigned long long part = 0;
+    rrow_pass<kBF16>(whole, l2_policy_normal(), [&](bool valid, float y, uint32_t, int) {
+      if (valid) part += fixed_mass(softmax_weight(y, M));
+    });
+    const unsigned long long tqx = rtopp_target(p, rblock_sum_u64(part, sm.red));
+    const Thresh th = rrow_select<kBF16, true>(whole, tqx, M, sm.hist, sm.red, sm.misc);
     unsigned long long rb2, first2;
     rrow_race_write<kBF16>(whole, th, M, eps, l2_policy_normal(), sm.red, &rb2, &first2);
     return static_cast<int32_t>(~static_cast<uint32_t>(rb2 ? rb2 : first2));
   }
-  const unsigned long long wl = sm.cw[L - 1];
-  const Thresh th{static_cast<uint32_t>(wl >> 32), static_cast<int32_t>(~static_cast<uint32_t>(wl))};
-  rlist_race(sm.cw, L, th, M, rc, eps, rb, first);
-  rblock_max2(rb, first, sm.red);
+  // race over the kept part of the boundary bin, with the same weights as pass B
+  {
+    float rbest = -1.0f;
+    int ridx = INT_MAX;
+    for (int i = threadIdx.x; i < total; i += kRT) {
+      const unsigned long long wd = sm.cw[i];
+      const uint32_t key = static_cast<uint32_t>(wd >> 32);
+      const int32_t idx = static_cast<int32_t>(~static_cast<uint32_t>(wd));
+      if (!kept_by(key, idx, bth.key, bth.idx)) continue;
+      const float y = kfloat(key);
+      const float wt = __fmul_rn(__fmul_rn(static_cast<float>(pweight(y, H).w24), 5.9604644775390625e-8f), fbf);
+      const float r = __fmul_rn(wt, rrcp_approx(__fadd_rn(__ldg(rc.q + idx), eps)));
+      if (r > rbest || (r == rbest && idx < ridx)) {
+        rbest = r;
+        ridx = idx;
+      }
+      if (rc.out) rc.out[idx] = y;
+    }
+    unsigned long long c = rbest >= 0.0f ? order_word(fkey(rbest), ridx) : 0ull;
+    c = c > rb ? c : rb;
+    unsigned long long dummy = 0;
+    rblock_max2(c, dummy, sm.red);
+    rb = c;
+  }
   if (rb) return static_cast<int32_t>(~static_cast<uint32_t>(rb));
   return rrow_first_max<kBF16>(whole, M, sm.red);  // every race quotient was NaN
 }
