@@ -343,11 +343,13 @@ __device__ void rbitonic_desc(unsigned long long* a, int N) {
 }
 
 // Moves the nonzero entries of a[0..kRCap) to the front, in order, and zero-fills the
-// rest; returns their count.
+// rest; returns their count.  Each thread reads a run of entries that other threads
+// wrote, so it starts with a barrier of its own.
 __device__ __noinline__ int rcompact_nonzero(unsigned long long* a, unsigned long long* red) {
   constexpr int per = kRCap / kRT;
   unsigned long long v[per];
   uint32_t c = 0;
+  __syncthreads();
 #pragma unroll
   for (int e = 0; e < per; ++e) {
     v[e] = a[per * threadIdx.x + e];
@@ -1234,35 +1236,57 @@ __device__ __noinline__ int32_t rrow_first_max(const RowCtx& rc, float M, unsign
 constexpr int kRPBins = 2048;           // mass bins of top-p-only rows: width 1/32 below H
 constexpr float kRPScale = 32.0f;
 
-// The weight of y against a reference H >= y: its bin b = floor(32 (H - y)) (kRPBins when
-// H - y >= 64, or y > H: no mass) and exp(-(H - y - b/32)), the weight relative to the bin
-// top, as an integer in units of 2^-24 (the difference H - y is carried exactly, so the
-// only error is the exponential's, about 2^-22 relative).  The mass of an element is
+// 2^x to about 2^-22 relative (the hardware approximation).
+__device__ __forceinline__ float rex2(float x) {
+  float r;
+  asm("ex2.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+constexpr float kLog2e = 1.4426950408889634f;
+
+// The reference H of a top-p-only row lies on the 1/32 grid (rounded up) with |H| < 2^18,
+// so every bin top H - b/32 (b < 2048) is a float exactly.  Rows whose H cannot (an
+// infinite or huge maximum) take the exact whole-row selection.
+__device__ __forceinline__ float pgrid_up(float h) {
+  return __fmul_rn(ceilf(__fmul_rn(h, kRPScale)), 1.0f / kRPScale);
+}
+__device__ __forceinline__ bool pgrid_ok(float h) { return fabsf(h) < 262144.0f; }  // false for NaN, inf
+
+// The bin factor exp(-b/32), to about 2^-22 relative: the exponent is split in double
+// into an integer power of two and a fraction, so the error does not grow with b.
+__device__ __forceinline__ float pfac(int b) {
+  const double z = static_cast<double>(b) * (1.4426950408889634074 / 32.0);
+  const double n = floor(z);
+  return __fmul_rn(rex2(-static_cast<float>(z - n)), __int_as_float((127 - static_cast<int>(n)) << 23));
+}
+
+// The weight of y against the reference H (on the grid, H >= y): its bin
+// b = floor(32 fl(H - y)) (kRPBins when that is not in [0, 2048): no mass) and the weight
+// relative to the bin top c = H - b/32 (exact), exp(-(c - y)) as an integer w24 in units
+// of 2^-24 (c - y is exact to 2^-30, so the only error is the exponential's, about 2^-22
+// relative; the top weight 2^24 is clamped to 2^24 - 1).  The mass of an element is
 // w24 * 2^-24 * exp(-b/32) against exp(H); every total, prefix and race below is taken in
-// this one arithmetic, so they agree with each other exactly.
+// this one arithmetic, so they agree with each other exactly.  The bin comes from the
+// rounded difference, so an element near a bin edge may fall on either side; its weight
+// follows its bin, and both passes see the same bin.
 struct PW {
   int b;
   uint32_t w24;
-  float frac;  // H - y - b/32, in [0, 1/32) up to rounding: the position inside the bin
+  float wf;    // w24 as a float (exact)
+  float frac;  // c - y, in [0, 1/32) up to the rounding of H - y: the position inside the bin
 };
 __device__ __forceinline__ PW pweight(float y, float H) {
-  // branch-free: every element of a warp takes the same instructions
-  const bool top = y == H;  // also covers +-inf maxima
-  const float d = top ? 0.0f : __fsub_rn(H, y);
-  const bool valid = d >= 0.0f && d < 64.0f;  // false for NaN and for y > H
-  const float bb = __fsub_rn(d, H);
-  const float dl0 = __fadd_rn(__fsub_rn(H, __fsub_rn(d, bb)), __fsub_rn(-y, bb));  // H - y = d + dl
-  const float dl = top ? 0.0f : dl0;
-  const float f = __fmul_rn(valid ? d : 0.0f, kRPScale);
-  const float t = __fadd_rd(f, 8388608.0f);  // floor(f) + 2^23
-  const int b = __float_as_int(t) - 0x4B000000;
-  const float frac = __fadd_rn(__fmul_rn(__fsub_rn(f, __fsub_rn(t, 8388608.0f)), 1.0f / kRPScale), dl);
-  const float v = __fmul_rn(__expf(-(valid ? frac : 0.0f)), 16777216.0f);  // an integer in [2^23, 2^24 + 2]
-  const uint32_t u = __float_as_uint(v);
+  const float d = __fsub_rn(H, y);
+  const float t = __fmaf_rd(d, kRPScale, 8388608.0f);  // floor(32 d) + 2^23 (exact product)
+  const uint32_t bu = __float_as_uint(t) - 0x4B000000u;
+  const float c = __fmaf_rn(__fsub_rn(t, 8388608.0f), -1.0f / kRPScale, H);
+  const float frac = __fsub_rn(c, y);
+  const float v = fminf(rex2(__fmaf_rn(frac, -kLog2e, 24.0f)), 16777215.0f);  // an integer in [2^23, 2^24)
   PW r;
-  r.b = valid ? b : kRPBins;
-  r.w24 = valid ? ((u & 0x7FFFFFu) | 0x800000u) << ((u >> 23) - 150u) : 0u;
-  r.frac = valid ? frac : 0.0f;
+  r.b = bu < static_cast<uint32_t>(kRPBins) ? static_cast<int>(bu) : kRPBins;
+  r.w24 = __float_as_uint(v) - 0x4A800000u;
+  r.wf = v;
+  r.frac = frac;
   return r;
 }
 
@@ -1273,39 +1297,67 @@ __device__ __forceinline__ int psub(const PW& w) {
   return rfloor_small(fminf(fmaxf(__fmul_rn(w.frac, kRPScale * kRPSub), 0.0f), static_cast<float>(kRPSub - 1)));
 }
 
+// Race quotient of an element of a top-p-only row before its bin factor: its weight
+// w24 / (q + eps) (reciprocal to about one ulp), as a key that is 0 for NaN or a negative
+// quotient and otherwise orders like the quotient.  The full quotient is this times
+// 2^-24 exp(-b/32), rounded once more, so the best of a bin is the bin's best key.
+__device__ __forceinline__ uint32_t prace_key(float wf, float q, float eps) {
+  const float u = __fmul_rn(wf, rrcp_approx(__fadd_rn(q, eps)));
+  return u >= 0.0f ? (__float_as_uint(u) & 0x7FFFFFFFu) + 1u : 0u;
+}
+__device__ __forceinline__ float prace_value(uint32_t key, float f24) {
+  return __fmul_rn(__uint_as_float(key - 1u), f24);
+}
+
+// The largest of a shared 64-bit word and w, kept in the word (a shared-window address);
+// the key in its high half is read first, so the common case, an element that does not
+// beat its bin's best, is one load and one compare.
+__device__ __forceinline__ void sh_max_word(uint32_t a, uint32_t key, unsigned long long w) {
+  uint32_t hi;
+  asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(hi) : "r"(a + 4u));
+  if (key >= hi) asm volatile("red.shared.max.u64 [%0], %1;" ::"r"(a), "l"(w) : "memory");
+}
+
 // Pass A of top-p-only rows over this CTA's part: the exact transformed values, binned
 // against H with their 24-bit weights summed per bin in two 12/13-bit limbs
-// (h[b], h[kRPBins + b]: a bin takes any row of at most 2^18 elements without overflow).
-// Returns the part's largest value as a key.
+// (h[b], h[kRPBins + b]: a bin takes any row of at most 2^18 elements without overflow),
+// and per bin the best race word (race key, index; the lower index on equal keys) in
+// ub[b].  Returns the part's largest value as a key.
 template <bool kBF16>
-__device__ __noinline__ unsigned long long rp_pass_a(const RowCtx& rc, float H, uint32_t* h, unsigned long long* red) {
+__device__ __noinline__ unsigned long long rp_pass_a(const RowCtx& rc, float H, float eps, uint32_t* h,
+                                                     unsigned long long* ub, unsigned long long* red) {
   constexpr int G = kBF16 ? 8 : 4;
+  constexpr int kUA = kBF16 ? 1 : 2;  // vectors in flight per thread (q rides along)
   const unsigned long long pol = l2_policy_last();
   const uint4* xr = rc.x;
+  const float4* qr = reinterpret_cast<const float4*>(rc.q);
   const int g0 = rc.g0, g1 = rc.g1;
   const uint32_t* bitmap = rc.bitmap;
   const bool pen_on = rc.pen_on, identity = rc.identity;
   const float pen = rc.pen;
   const FixedDivisor dv = rc.div;
   for (int i = threadIdx.x; i < 2 * kRPBins; i += kRT) h[i] = 0u;
+  for (int i = threadIdx.x; i < kRPBins; i += kRT) ub[i] = 0ull;
   __syncthreads();
-  unsigned long long kmax = 0;
-  for (int base = g0; base < g1; base += kRT * kRU) {
-    uint4 w[kRU];
+  float ymax = -INFINITY;
+  for (int base = g0; base < g1; base += kRT * kUA) {
+    uint4 w[kUA];
+    float4 qv[kUA][G / 4];
 #pragma unroll
-    for (int u = 0; u < kRU; ++u) {
+    for (int u = 0; u < kUA; ++u) {
       const int g = base + u * kRT + static_cast<int>(threadIdx.x);
       w[u] = g < g1 ? ld_row16(xr + g, pol) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int hh = 0; hh < G / 4; ++hh)
+        qv[u][hh] = g < g1 ? __ldcs(qr + g * (G / 4) + hh) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int u = 0; u < kRU; ++u) {
+    for (int u = 0; u < kUA; ++u) {
       const int g = base + u * kRT + static_cast<int>(threadIdx.x);
       if (g >= g1) continue;
       float v[G];
       unpack16<kBF16>(w[u], v);
       const uint32_t bits = rseen_bits<G>(bitmap, pen_on, g);
-#pragma unroll
-      for (int e = 0; e < G; ++e) v[e] = isnan(v[e]) ? -INFINITY : v[e];
       if (bits) {
 #pragma unroll
         for (int e = 0; e < G; ++e)
@@ -1313,66 +1365,66 @@ __device__ __noinline__ unsigned long long rp_pass_a(const RowCtx& rc, float H, 
       }
 #pragma unroll
       for (int e = 0; e < G; ++e) {
+        // a NaN logit stays NaN here: it has no bin, no race and no part in the maximum,
+        // exactly as the -inf it stands for
         const float y = __fadd_rn(identity ? v[e] : rdiv(v[e], dv), 0.0f);
-        const unsigned long long ky = fkey(y);
-        kmax = ky > kmax ? ky : kmax;
+        ymax = fmaxf(ymax, y);
         const PW pw = pweight(y, H);
         if (pw.b < kRPBins) {
           sh_red_add(&h[pw.b], pw.w24 & 0xFFFu);
           sh_red_add(&h[kRPBins + pw.b], pw.w24 >> 12);
+          const float4 q4 = qv[u][e / 4];
+          const float qe = (e & 3) == 0 ? q4.x : (e & 3) == 1 ? q4.y : (e & 3) == 2 ? q4.z : q4.w;
+          const uint32_t key = prace_key(pw.wf, qe, eps);
+          sh_max_word(smem_u32(ub + pw.b), key, order_word(key, g * G + e));
         }
       }
     }
   }
-  unsigned long long dummy = 0;
+  unsigned long long kmax = fkey(__fadd_rn(ymax, 0.0f)), dummy = 0;
   rblock_max2(kmax, dummy, red);
   return kmax;
 }
 
-// Pass B of top-p-only rows over this CTA's part: every element in a bin above bstar is
-// kept (raced with its weight from pass A's arithmetic, written); bin bstar goes to the
-// warps' segments of cw; the rest is written as -inf.  ftab[b] = exp(-b/32).  *rb: the
-// block's best race word.
-constexpr int kRUB = 2;  // loads in flight per thread in pass B (its registers go to the arithmetic)
+// Pass B of top-p-only rows over this CTA's part, once the boundary bin bstar is known:
+// an element in a bin above it (H - y < bstar / 32) is kept and written; one of bin
+// bstar goes to its warp's segment of cw (its key and index); the rest is written as
+// -inf.  The race over the kept bins is already decided by pass A's per-bin words.
+// Returns the warp's segment count.
 template <bool kBF16>
-__device__ __noinline__ void rp_pass_b(const RowCtx& rc, float H, int bstar, const float* ftab, float eps,
-                                       unsigned long long* cw, unsigned long long* rb_out, uint32_t* wcnt_out) {
+__device__ __noinline__ uint32_t rp_pass_b(const RowCtx& rc, float H, int bstar, unsigned long long* cw) {
   constexpr int G = kBF16 ? 8 : 4;
+  constexpr int kUB = kBF16 ? 2 : 4;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const unsigned lt = (1u << lane) - 1u;
   unsigned long long* seg = cw + warp * kRSeg;
   const unsigned long long pol = l2_policy_first();
   const uint4* xr = rc.x;
-  const float* qr = rc.q;
   float* out = rc.out;
   const int g0 = rc.g0, g1 = rc.g1;
   const uint32_t* bitmap = rc.bitmap;
   const bool pen_on = rc.pen_on, identity = rc.identity;
   const float pen = rc.pen;
   const FixedDivisor dv = rc.div;
-  float rbest = -1.0f;  // best race quotient so far and its index (ties: lower index)
-  int ridx = INT_MAX;
+  // bin b = floor(32 d) with d = fl(H - y) is taken on an exact multiple of d, so
+  // b < bstar exactly when d < bstar / 32
+  const float clo = static_cast<float>(bstar) * (1.0f / kRPScale);
+  const float chi = bstar < kRPBins ? static_cast<float>(bstar + 1) * (1.0f / kRPScale) : clo;
   uint32_t wcnt = 0;
-  for (int base = g0; base < g1; base += kRT * kRUB) {
-    uint4 w[kRUB];
-    float4 qv[kRUB][G / 4];  // q of the same elements, loaded with them
+  for (int base = g0; base < g1; base += kRT * kUB) {
+    uint4 w[kUB];
 #pragma unroll
-    for (int u = 0; u < kRUB; ++u) {
+    for (int u = 0; u < kUB; ++u) {
       const int g = base + u * kRT + static_cast<int>(threadIdx.x);
       w[u] = g < g1 ? ld_row16(xr + g, pol) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-      for (int hh = 0; hh < G / 4; ++hh)
-        qv[u][hh] = g < g1 ? __ldcs(reinterpret_cast<const float4*>(qr) + g * (G / 4) + hh) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int u = 0; u < kRUB; ++u) {
+    for (int u = 0; u < kUB; ++u) {
       const int g = base + u * kRT + static_cast<int>(threadIdx.x);
       const bool in = g < g1;
       float v[G];
       unpack16<kBF16>(w[u], v);
       const uint32_t bits = in ? rseen_bits<G>(bitmap, pen_on, g) : 0u;
-#pragma unroll
-      for (int e = 0; e < G; ++e) v[e] = isnan(v[e]) ? -INFINITY : v[e];
       if (__any_sync(kFull, bits != 0u)) {
 #pragma unroll
         for (int e = 0; e < G; ++e)
@@ -1381,22 +1433,10 @@ __device__ __noinline__ void rp_pass_b(const RowCtx& rc, float H, int bstar, con
       uint32_t kmask = 0, bmask = 0;
 #pragma unroll
       for (int e = 0; e < G; ++e) {
-        v[e] = __fadd_rn(identity ? v[e] : rdiv(v[e], dv), 0.0f);
-        const PW pw = pweight(v[e], H);
-        const bool kept = in && pw.b < bstar;
-        kmask |= (kept ? 1u : 0u) << e;
-        bmask |= (in && pw.b == bstar ? 1u : 0u) << e;
-        // the race, branch-free: the quotient to about one ulp (only near-ties can change);
-        // a thread meets its elements in increasing index order, so a strict > keeps the
-        // lower index
-        const float wt = __fmul_rn(__fmul_rn(static_cast<float>(pw.w24), 5.9604644775390625e-8f),
-                                   ftab[pw.b < kRPBins ? pw.b : kRPBins - 1]);
-        const float4 q4 = qv[u][e / 4];
-        const float qe = (e & 3) == 0 ? q4.x : (e & 3) == 1 ? q4.y : (e & 3) == 2 ? q4.z : q4.w;
-        const float r = __fmul_rn(wt, rrcp_approx(__fadd_rn(qe, eps)));
-        const bool better = kept && r > rbest;  // false for NaN
-        rbest = better ? r : rbest;
-        ridx = better ? g * G + e : ridx;
+        v[e] = __fadd_rn(identity ? v[e] : rdiv(v[e], dv), 0.0f);  // NaN: neither kept nor in the band
+        const float d = __fsub_rn(H, v[e]);
+        kmask |= (in && d < clo ? 1u : 0u) << e;
+        bmask |= (in && d >= clo && d < chi ? 1u : 0u) << e;
       }
       if (__any_sync(kFull, bmask != 0u)) {
 #pragma unroll
@@ -1422,8 +1462,7 @@ __device__ __noinline__ void rp_pass_b(const RowCtx& rc, float H, int bstar, con
       }
     }
   }
-  *rb_out = rbest >= 0.0f ? order_word(fkey(rbest), ridx) : 0ull;
-  *wcnt_out = wcnt;
+  return wcnt;
 }
 
 // Top-p-only (topp true) and keep-all rows, shared by the CTAs of team tm; rc covers this
@@ -1436,9 +1475,8 @@ __device__ __noinline__ int32_t rwide_row(const RowCtx& rc, const RowSmem& sm, c
   RowCtx whole = rc;
   whole.g0 = 0;
   whole.g1 = rc.nv;
-  if (exact) {
-    // the exact whole-row selection only, by rank 0 alone
-    if (tm.rank != 0) return -1;
+  // the exact whole-row selection, by rank 0 alone (the other members leave the row)
+  auto exact_row = [&]() -> int32_t {
     const float M = rmax_transformed(rrow_max_key<kBF16>(whole, l2_policy_last(), sm.red), whole);
     Thresh th{0u, INT_MAX};
     if (topp) {
@@ -1452,7 +1490,8 @@ __device__ __noinline__ int32_t rwide_row(const RowCtx& rc, const RowSmem& sm, c
     unsigned long long rb, first;
     rrow_race_write<kBF16>(whole, th, M, eps, l2_policy_normal(), sm.red, &rb, &first);
     return static_cast<int32_t>(~static_cast<uint32_t>(rb ? rb : first));
-  }
+  };
+  if (exact) return tm.rank == 0 ? exact_row() : -1;
   if (!topp) {
     // keep-all: the maximum, then the race and the write of every part
     tm.push(sm.misc, 0, rrow_max_key<kBF16>(rc, l2_policy_last(), sm.red));
@@ -1482,22 +1521,26 @@ __device__ __noinline__ int32_t rwide_row(const RowCtx& rc, const RowSmem& sm, c
     tm.sync();
     H = rmax_transformed(tm.max_of(sm.misc, 0), rc);
   }
+  H = pgrid_up(H);
+  if (!pgrid_ok(H)) return tm.rank == 0 ? exact_row() : -1;  // the same decision in every member
   // pass A; again with H = M when the sample missed the top of the row by more than the headroom
-  tm.push(sm.misc, 1, rp_pass_a<kBF16>(rc, H, sm.hist, sm.red));
+  tm.push(sm.misc, 1, rp_pass_a<kBF16>(rc, H, eps, sm.hist, sm.cw, sm.red));
   tm.sync();
   const float M = kfloat(static_cast<uint32_t>(tm.max_of(sm.misc, 1)));
   if (M > H) {
-    H = M;
+    H = pgrid_up(M);
     tm.sync();  // every member has read slot 1 and is done with the sample
-    tm.push(sm.misc, 1, rp_pass_a<kBF16>(rc, H, sm.hist, sm.red));
+    if (!pgrid_ok(H)) return tm.rank == 0 ? exact_row() : -1;
+    tm.push(sm.misc, 1, rp_pass_a<kBF16>(rc, H, eps, sm.hist, sm.cw, sm.red));
     tm.sync();
   }
   // bin factors exp(-b/32), the bin masses summed over the members, their total S, and
   // the bin bstar holding the boundary (its prefix reaches p * S)
   float* ftab = reinterpret_cast<float*>(sm.wbuf);
-  for (int b = threadIdx.x; b < kRPBins; b += kRT) ftab[b] = __expf(-static_cast<float>(b) * (1.0f / kRPScale));
+  for (int b = threadIdx.x; b < kRPBins; b += kRT) ftab[b] = pfac(b);
   double above = 0.0, tq = 0.0;
   int bstar;
+  unsigned long long ubest[kRPBins / kRT];  // the best race word of each of this thread's bins
   {
     constexpr int per = kRPBins / kRT;
     double m[per];
@@ -1505,13 +1548,15 @@ __device__ __noinline__ int32_t rwide_row(const RowCtx& rc, const RowSmem& sm, c
 #pragma unroll
     for (int e = 0; e < per; ++e) {
       const int b = per * static_cast<int>(threadIdx.x) + e;
-      unsigned long long c = 0;
+      unsigned long long c = 0, wb = 0;
       for (int r = 0; r < tm.C; ++r) {
         const uint32_t* hr = tm.remote(sm.hist, r);
+        const unsigned long long x = tm.remote(sm.cw, r)[b];
         c += static_cast<unsigned long long>(hr[b]) + (static_cast<unsigned long long>(hr[kRPBins + b]) << 12);
+        wb = x > wb ? x : wb;
       }
-      m[e] = static_cast<double>(c) * 5.9604644775390625e-8 *
-             static_cast<double>(__expf(-static_cast<float>(b) * (1.0f / kRPScale)));
+      ubest[e] = wb;
+      m[e] = static_cast<double>(c) * 5.9604644775390625e-8 * static_cast<double>(pfac(b));
       sum += m[e];
     }
     if (threadIdx.x == 0) sm.misc[kMBin] = static_cast<unsigned long long>(kRPBins);
@@ -1550,15 +1595,30 @@ __device__ __noinline__ int32_t rwide_row(const RowCtx& rc, const RowSmem& sm, c
       }
       acc = after;
     }
-    tm.sync();  // every member is done reading the histograms and the slots
+    __syncthreads();
     bstar = static_cast<int>(sm.misc[kMBin]);
     above = reinterpret_cast<const double*>(sm.misc)[kMAbove];
   }
+  // the race over the bins above the boundary bin (rank 0): each bin's best key scaled by
+  // the bin's factor, with the index of its element
+  unsigned long long rb = 0;
+  if (tm.rank == 0) {
+#pragma unroll
+    for (int e = 0; e < kRPBins / kRT; ++e) {
+      const int b = (kRPBins / kRT) * static_cast<int>(threadIdx.x) + e;
+      if (b < bstar && ubest[e]) {
+        const float rv = prace_value(static_cast<uint32_t>(ubest[e] >> 32), __fmul_rn(ftab[b], 5.9604644775390625e-8f));
+        const unsigned long long c = order_word(fkey(rv), static_cast<int32_t>(~static_cast<uint32_t>(ubest[e])));
+        rb = c > rb ? c : rb;
+      }
+    }
+    unsigned long long dummy = 0;
+    rblock_max2(rb, dummy, sm.red);
+  }
+  tm.sync();  // every member is done reading the histograms, the per-bin words and the slots
 
   // pass B over this CTA's part
-  unsigned long long rb;
-  uint32_t wcnt;
-  rp_pass_b<kBF16>(rc, H, bstar, ftab, eps, sm.cw, &rb, &wcnt);
+  const uint32_t wcnt = rp_pass_b<kBF16>(rc, H, bstar, sm.cw);
   if (lane == 0) segcnt[warp] = wcnt;
   __syncthreads();
   bool over = false;
@@ -1568,13 +1628,9 @@ __device__ __noinline__ int32_t rwide_row(const RowCtx& rc, const RowSmem& sm, c
     const int w = i / kRSeg;
     if (i - w * kRSeg >= static_cast<int>(segcnt[w])) sm.cw[i] = 0ull;
   }
-  unsigned long long first = 0;
-  rblock_max2(rb, first, sm.red);
   const int nb = over ? kRCap + 1 : rcompact_nonzero(sm.cw, sm.red);
-  tm.push(sm.misc, 4, rb);
   tm.push(sm.misc, 6, static_cast<unsigned long long>(nb));
   tm.sync();
-  rb = tm.max_of(sm.misc, 4);
   int total = 0;
   bool fits = bstar < kRPBins;
   for (int r = 0; r < tm.C; ++r) {
@@ -1765,8 +1821,9 @@ __device__ __noinline__ int32_t rwide_row(const RowCtx& rc, const RowSmem& sm, c
     rrow_race_write<kBF16>(whole, th, M, eps, l2_policy_normal(), sm.red, &rb2, &first2);
     return static_cast<int32_t>(~static_cast<uint32_t>(rb2 ? rb2 : first2));
   }
-  // race over the kept part of the boundary bin, with the same weights as pass B
+  // race over the kept part of the boundary bin, in pass A's arithmetic
   {
+    const float f24b = __fmul_rn(fbf, 5.9604644775390625e-8f);
     float rbest = -1.0f;
     int ridx = INT_MAX;
     for (int i = threadIdx.x; i < total; i += kRT) {
@@ -1775,9 +1832,9 @@ __device__ __noinline__ int32_t rwide_row(const RowCtx& rc, const RowSmem& sm, c
       const int32_t idx = static_cast<int32_t>(~static_cast<uint32_t>(wd));
       if (!kept_by(key, idx, bth.key, bth.idx)) continue;
       const float y = kfloat(key);
-      const float wt = __fmul_rn(__fmul_rn(static_cast<float>(pweight(y, H).w24), 5.9604644775390625e-8f), fbf);
-      const float r = __fmul_rn(wt, rrcp_approx(__fadd_rn(__ldg(rc.q + idx), eps)));
-      if (r > rbest || (r == rbest && idx < ridx)) {
+      const uint32_t rk = prace_key(pweight(y, H).wf, __ldg(rc.q + idx), eps);
+      const float r = rk ? prace_value(rk, f24b) : -1.0f;
+      if (rk && (r > rbest || (r == rbest && idx < ridx))) {
         rbest = r;
         ridx = idx;
       }
