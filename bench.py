@@ -269,6 +269,9 @@ def main():
             step()
     stream.synchronize()
     kernel_name = kps.last_kernel()
+    launches_per_step = kps.last_launch_count()
+    if launches_per_step == 2:
+        kernel_name = "kps_prepass_kernel+" + kernel_name
 
     # ---- device-resident timed region --------------------------------------------------------
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -379,7 +382,7 @@ def main():
         "clocks": clk,
         "e2e": {"value": e2e_rows, "unit": "rows/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * launches_per_step,
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": traffic,
                      "peak_source": peaks["source"], "kernel": kernel_name,

@@ -57,6 +57,8 @@ def load_library() -> ctypes.CDLL:
     lib.kps_get_kernel_policy.argtypes = []
     lib.kps_last_kernel.restype = I32
     lib.kps_last_kernel.argtypes = []
+    lib.kps_last_launch_count.restype = I32
+    lib.kps_last_launch_count.argtypes = []
     lib.kps_query_launch.restype = I32
     lib.kps_query_launch.argtypes = [I64, I64, I32, ctypes.POINTER(I32), ctypes.POINTER(I64),
                                      ctypes.POINTER(ctypes.c_size_t)]
@@ -122,6 +124,11 @@ KERNEL_NAMES = {1: "kps_sample_kernel", 2: "kps_row_kernel"}
 def last_kernel() -> str:
     """Name of the kernel this thread's most recent launching sample() call used ("" if none)."""
     return KERNEL_NAMES.get(int(load_library().kps_last_kernel()), "")
+
+
+def last_launch_count() -> int:
+    """Kernels this thread's most recent launching sample() call queued (2: pre-pass + row kernel)."""
+    return int(load_library().kps_last_launch_count())
 
 
 def query_launch(B: int, V: int, dtype: torch.dtype = torch.float32) -> dict:

@@ -116,6 +116,8 @@ struct Params {
   int use_tma;  // every row of logits, q and out starts on a 16-byte boundary
   int filter;   // rows this launch takes: 0 all, 1 top-k/one-element rows, 2 the others
   int exact;    // row kernel: skip the sample and the band, always select over the whole row
+  unsigned char* pre;  // row kernel: per-row records of the pre-pass (nullptr: no pre-pass)
+  int pre_rows;        // records available (the first pre_rows top-p-only rows use them)
 };
 
 constexpr int kMaxRowList = 256;  // rows one worker (CTA or cluster) may own in a filtered launch
@@ -1651,11 +1653,22 @@ static kps_status choose_launch(int64_t B, int64_t V, LaunchCfg* out) {
 
 // The kernel the calling thread's last successful kps_sample launched (1 cluster, 2 row).
 static thread_local int t_last_kernel = 0;
+static thread_local int t_last_launches = 0;
 
 // Kernel choice: 0 = automatic, 1 = cluster kernel only, 2 = row kernel where supported,
 // 3 = row kernel with the exact whole-row selection forced (a test hook).
 static int g_policy = 0;
 constexpr int64_t kRowMinRows = 64;  // automatic: the row kernel from this batch size up
+constexpr size_t kWorkspaceMin = 256;  // the status word (and its alignment)
+constexpr int64_t kMaxPreRows = 1024;  // top-p-only rows with a pre-pass record, at most
+
+// Pre-pass records a workspace of `bytes` holds for a batch of B rows.
+inline int64_t pre_rows_for(int64_t B, int64_t V, size_t bytes) {
+  if (V <= kRKeepAllV || bytes <= kWorkspaceMin) return 0;
+  int64_t n = static_cast<int64_t>((bytes - kWorkspaceMin) / kPRecBytes);
+  n = n < B ? n : B;
+  return n < kMaxPreRows ? n : kMaxPreRows;
+}
 
 constexpr int kRowTeams[] = {2, 1};  // cluster sizes tried, widest first: CTAs sharing a top-p-only row
 
@@ -1680,6 +1693,11 @@ static cudaError_t prepare_row_kernel() {
   if (err != cudaSuccess) return err;
   const int optin = device_smem_optin() - static_cast<int>(fa.sharedSizeBytes);
   err = cudaFuncSetAttribute(kps_row_kernel<kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+  if (err != cudaSuccess) return err;
+  err = cudaFuncGetAttributes(&fa, kps_prepass_kernel<kBF16>);
+  if (err != cudaSuccess) return err;
+  const int optin2 = device_smem_optin() - static_cast<int>(fa.sharedSizeBytes);
+  err = cudaFuncSetAttribute(kps_prepass_kernel<kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin2);
   if (err == cudaSuccess) done[dev] = true;
   return err;
 }
@@ -1786,7 +1804,9 @@ extern "C" {
 
 size_t kps_workspace_size(int64_t B, int64_t V, kps_dtype dt) {
   if (B < 0 || V < 1 || (dt != KPS_F32 && dt != KPS_BF16)) return 0;
-  return 256;
+  if (V <= kps::kRKeepAllV) return kps::kWorkspaceMin;
+  const int64_t rows = B < kps::kMaxPreRows ? B : kps::kMaxPreRows;
+  return kps::kWorkspaceMin + static_cast<size_t>(rows) * kps::kPRecBytes;
 }
 
 int64_t kps_max_vocab(kps_dtype dt) {
@@ -1835,8 +1855,7 @@ kps_status kps_sample(const void* logits, kps_dtype dt, int64_t B, int64_t V, co
   if (dt != KPS_F32 && dt != KPS_BF16) return KPS_ERR_INVALID_ARG;
   if (V < 1 || V > INT32_MAX || B < 0) return KPS_ERR_INVALID_ARG;
   if (!(eps >= 0.0f) || std::isinf(eps)) return KPS_ERR_INVALID_ARG;
-  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
-      workspace_bytes < kps_workspace_size(B, V, dt))
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < kps::kWorkspaceMin)
     return KPS_ERR_WORKSPACE;
   if (B == 0) return KPS_OK;
   if (B > INT32_MAX / 16) return KPS_ERR_INVALID_ARG;
@@ -1883,8 +1902,30 @@ kps_status kps_sample(const void* logits, kps_dtype dt, int64_t B, int64_t V, co
   P.use_tma = aligned ? 1 : 0;
   P.filter = 0;
   P.exact = kps::g_policy == 3 ? 1 : 0;
+  P.pre = nullptr;
+  P.pre_rows = 0;
 
   if (use_row) {
+    // the pre-pass pays when rows outnumber the clusters (then the top-k rows come C to a
+    // cluster and a top-p-only row would keep its pair of CTAs busy the longest); with
+    // fewer rows every row has a cluster of its own from the start
+    const int64_t pre_rows = (P.exact || B <= rcfg.clusters) ? 0 : kps::pre_rows_for(B, V, workspace_bytes);
+    if (pre_rows > 0) {
+      // pass A of the top-p-only rows first, over the whole resident grid
+      P.pre = static_cast<unsigned char*>(workspace) + kps::kWorkspaceMin;
+      P.pre_rows = static_cast<int>(pre_rows);
+      cudaLaunchConfig_t pl = {};
+      pl.gridDim = dim3(static_cast<unsigned>(rcfg.clusters * rcfg.cs));
+      pl.blockDim = dim3(kps::kRT);
+      pl.dynamicSmemBytes = rcfg.smem;
+      pl.stream = stream;
+      cudaError_t e = dt == KPS_BF16 ? cudaLaunchKernelEx(&pl, kps::kps_prepass_kernel<true>, P)
+                                     : cudaLaunchKernelEx(&pl, kps::kps_prepass_kernel<false>, P);
+      if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return KPS_ERR_CUDA;
+      }
+    }
     // a persistent grid of resident clusters; a cluster's CTAs share the top-p-only and
     // keep-all rows and take the other rows one each
     const int64_t ncl = B < rcfg.clusters ? B : rcfg.clusters;
@@ -1893,13 +1934,17 @@ kps_status kps_sample(const void* logits, kps_dtype dt, int64_t B, int64_t V, co
     rl.blockDim = dim3(kps::kRT);
     rl.dynamicSmemBytes = rcfg.smem;
     rl.stream = stream;
-    cudaLaunchAttribute rattr[1];
+    cudaLaunchAttribute rattr[2];
     rattr[0].id = cudaLaunchAttributeClusterDimension;
     rattr[0].val.clusterDim.x = rcfg.cs;
     rattr[0].val.clusterDim.y = 1;
     rattr[0].val.clusterDim.z = 1;
+    // after a pre-pass: start at once (programmatic dependent launch); only the rows that
+    // read its records wait for it
+    rattr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    rattr[1].val.programmaticStreamSerializationAllowed = 1;
     rl.attrs = rattr;
-    rl.numAttrs = 1;
+    rl.numAttrs = P.pre ? 2 : 1;
     cudaError_t e = dt == KPS_BF16 ? cudaLaunchKernelEx(&rl, kps::kps_row_kernel<true>, P)
                                    : cudaLaunchKernelEx(&rl, kps::kps_row_kernel<false>, P);
     if (e != cudaSuccess) {
@@ -1907,6 +1952,7 @@ kps_status kps_sample(const void* logits, kps_dtype dt, int64_t B, int64_t V, co
       return KPS_ERR_CUDA;
     }
     kps::t_last_kernel = 2;
+    kps::t_last_launches = P.pre ? 2 : 1;
     return KPS_OK;
   }
 
@@ -1930,6 +1976,7 @@ kps_status kps_sample(const void* logits, kps_dtype dt, int64_t B, int64_t V, co
     return KPS_ERR_CUDA;
   }
   kps::t_last_kernel = 1;
+  kps::t_last_launches = 1;
   return KPS_OK;
 }
 
@@ -1942,6 +1989,8 @@ kps_status kps_set_kernel_policy(int policy) {
 int kps_get_kernel_policy(void) { return kps::g_policy; }
 
 int kps_last_kernel(void) { return kps::t_last_kernel; }
+
+int kps_last_launch_count(void) { return kps::t_last_launches; }
 
 kps_status kps_last_device_status(void* workspace, cudaStream_t stream, int* out) {
   if (!workspace || !out) return KPS_ERR_INVALID_ARG;
@@ -1991,9 +2040,8 @@ extern "C" kps_status kps_sample_noalloc(const void* logits, kps_dtype dt, int64
                                          const int32_t* seen_indptr, const int32_t* seen_ids,
                                          const float* penalty, const float* q, float eps, int need_logits,
                                          int64_t* out_idx, float* out_filtered, cudaStream_t stream) {
-  const size_t need = kps_workspace_size(B, V, dt);
-  if (need == 0) return KPS_ERR_INVALID_ARG;
-  if (need > kps::kNoallocScratchBytes) return KPS_ERR_UNSUPPORTED;
+  if (kps_workspace_size(B, V, dt) == 0) return KPS_ERR_INVALID_ARG;
+  const size_t need = kps::kWorkspaceMin;  // the status word; no room for pre-pass records
   if (B == 0) return KPS_OK;
   void* scratch = kps::noalloc_scratch_address();
   if (!scratch) return KPS_ERR_CUDA;
@@ -2003,5 +2051,5 @@ extern "C" kps_status kps_sample_noalloc(const void* logits, kps_dtype dt, int64
     return KPS_ERR_CUDA;
   }
   return kps_sample(logits, dt, B, V, top_k, top_p, temperature, seen_indptr, seen_ids, penalty, q, eps,
-                    need_logits, out_idx, out_filtered, scratch, kps::kNoallocScratchBytes, stream);
+                    need_logits, out_idx, out_filtered, scratch, need, stream);
 }

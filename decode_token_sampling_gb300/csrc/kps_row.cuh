@@ -1465,11 +1465,62 @@ __device__ __noinline__ uint32_t rp_pass_b(const RowCtx& rc, float H, int bstar,
   return wcnt;
 }
 
+// ---- the pre-pass record of a top-p-only row --------------------------------------------
+//
+// With a workspace large enough, pass A of the top-p-only rows runs before the row kernel
+// in a kernel of its own (kps_prepass_kernel) that spreads every such row over many CTAs.
+// They merge their bin sums and per-bin race words into the row's record with global
+// atomics; the row kernel reads the record instead of running pass A, and zeroes it for
+// the next launch.
+constexpr size_t kPRecBytes = 32896;  // sums u64[2048], race words u64[2048], M, H, padding
+constexpr int kPreMaxChunks = 16;     // CTAs of the pre-pass per row, at most
+
+struct PRec {
+  unsigned long long* sums;  // per bin: the sum of w24 over the row
+  unsigned long long* ub;    // per bin: the best race word
+  unsigned long long* M;     // the row's largest value as a key
+  uint32_t* H;               // the reference H (float bits)
+};
+__device__ __forceinline__ PRec prec_at(const Params& P, int j) {
+  unsigned char* b = P.pre + static_cast<size_t>(j) * kPRecBytes;
+  return PRec{reinterpret_cast<unsigned long long*>(b), reinterpret_cast<unsigned long long*>(b + 16384),
+              reinterpret_cast<unsigned long long*>(b + 32768), reinterpret_cast<uint32_t*>(b + 32776)};
+}
+
+// Rows whose pass A the pre-pass takes: top-p-only rows of a row past the keep-all size,
+// outside exact mode.  Every kernel agrees on it.
+__device__ __forceinline__ bool row_prepass(const Params& P, int64_t r) {
+  if (P.exact || P.V <= kRKeepAllV || row_is_kmode(P, r)) return false;
+  const float p = P.top_p[r];
+  return !isnan(p) && p < 1.0f;
+}
+
+// Rows r' < r with row_prepass (the ordinal of row r among them); block-wide.
+__device__ int prepass_ordinal(const Params& P, int64_t r, unsigned long long* red) {
+  unsigned long long c = 0;
+  for (int64_t i = threadIdx.x; i < r; i += kRT) c += row_prepass(P, i) ? 1ull : 0ull;
+  return static_cast<int>(rblock_sum_u64(c, red));
+}
+
+// The zeroed state every record is left in: this member's share of it (members split the
+// bins; rank 0 takes M and H).
+__device__ __forceinline__ void prec_clear(const PRec& rec, const Team& tm) {
+  const int b0 = kRPBins * tm.rank / tm.C, b1 = kRPBins * (tm.rank + 1) / tm.C;
+  for (int b = b0 + static_cast<int>(threadIdx.x); b < b1; b += kRT) {
+    rec.sums[b] = 0ull;
+    rec.ub[b] = 0ull;
+  }
+  if (tm.rank == 0 && threadIdx.x == 0) {
+    *rec.M = 0ull;
+    *rec.H = 0u;
+  }
+}
+
 // Top-p-only (topp true) and keep-all rows, shared by the CTAs of team tm; rc covers this
 // CTA's part.  Returns the chosen index on the team's rank 0 (-1 elsewhere).
 template <bool kBF16>
 __device__ __noinline__ int32_t rwide_row(const RowCtx& rc, const RowSmem& sm, const Team& tm, bool topp, float p,
-                                          float eps, bool exact) {
+                                          float eps, bool exact, const PRec* rec) {
   uint32_t* segcnt = reinterpret_cast<uint32_t*>(sm.misc + kMSeg);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   RowCtx whole = rc;
@@ -1507,32 +1558,58 @@ __device__ __noinline__ int32_t rwide_row(const RowCtx& rc, const RowSmem& sm, c
     return tm.rank == 0 ? static_cast<int32_t>(~static_cast<uint32_t>(c)) : -1;
   }
 
-  // reference H: the sample maximum + headroom (every member samples the same elements)
-  float H;
-  if (rc.V > kRKeepAllV) {
-    uint32_t* samp = reinterpret_cast<uint32_t*>(sm.wbuf);
-    rsample_load<kBF16>(whole, samp);
-    unsigned long long a = 0, b = 0;
-    for (int i = threadIdx.x; i < kRSamp; i += kRT) a = samp[i] > a ? samp[i] : a;
-    rblock_max2(a, b, sm.red);
-    H = __fadd_rn(kfloat(static_cast<uint32_t>(a)), kRHeadroom);
+  // reference H: the sample maximum + headroom (every member samples the same elements),
+  // or the pre-pass's, with its pass A
+  float H, Mr = 0.0f;
+  bool from_rec = false;  // bins and race words come from the pre-pass record
+  if (rec) {
+    // the pre-pass runs as the prerequisite grid of this launch: wait for its records
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    H = __uint_as_float(__ldcg(rec->H));
+    Mr = kfloat(static_cast<uint32_t>(__ldcg(rec->M)));
+    tm.sync();  // every member has read H and M before the record is cleared
+    if (!pgrid_ok(H) || Mr > H) {
+      // no pass A in the record, or the sample missed the top of the row: clear it and
+      // go on as without one
+      prec_clear(*rec, tm);
+      if (!pgrid_ok(H)) return tm.rank == 0 ? exact_row() : -1;
+      H = pgrid_up(Mr);
+      if (!pgrid_ok(H)) return tm.rank == 0 ? exact_row() : -1;
+      rec = nullptr;
+    } else {
+      from_rec = true;
+    }
   } else {
-    tm.push(sm.misc, 0, rrow_max_key<kBF16>(rc, l2_policy_last(), sm.red));
-    tm.sync();
-    H = rmax_transformed(tm.max_of(sm.misc, 0), rc);
+    if (rc.V > kRKeepAllV) {
+      uint32_t* samp = reinterpret_cast<uint32_t*>(sm.wbuf);
+      rsample_load<kBF16>(whole, samp);
+      unsigned long long a = 0, b = 0;
+      for (int i = threadIdx.x; i < kRSamp; i += kRT) a = samp[i] > a ? samp[i] : a;
+      rblock_max2(a, b, sm.red);
+      H = __fadd_rn(kfloat(static_cast<uint32_t>(a)), kRHeadroom);
+    } else {
+      tm.push(sm.misc, 0, rrow_max_key<kBF16>(rc, l2_policy_last(), sm.red));
+      tm.sync();
+      H = rmax_transformed(tm.max_of(sm.misc, 0), rc);
+    }
+    H = pgrid_up(H);
+    if (!pgrid_ok(H)) return tm.rank == 0 ? exact_row() : -1;  // the same decision in every member
   }
-  H = pgrid_up(H);
-  if (!pgrid_ok(H)) return tm.rank == 0 ? exact_row() : -1;  // the same decision in every member
-  // pass A; again with H = M when the sample missed the top of the row by more than the headroom
-  tm.push(sm.misc, 1, rp_pass_a<kBF16>(rc, H, eps, sm.hist, sm.cw, sm.red));
-  tm.sync();
-  const float M = kfloat(static_cast<uint32_t>(tm.max_of(sm.misc, 1)));
-  if (M > H) {
-    H = pgrid_up(M);
-    tm.sync();  // every member has read slot 1 and is done with the sample
-    if (!pgrid_ok(H)) return tm.rank == 0 ? exact_row() : -1;
+  float M;
+  if (from_rec) {
+    M = Mr;
+  } else {
+    // pass A; again with H = M when the sample missed the top of the row by more than the headroom
     tm.push(sm.misc, 1, rp_pass_a<kBF16>(rc, H, eps, sm.hist, sm.cw, sm.red));
     tm.sync();
+    M = kfloat(static_cast<uint32_t>(tm.max_of(sm.misc, 1)));
+    if (M > H) {
+      H = pgrid_up(M);
+      tm.sync();  // every member has read slot 1 and is done with the sample
+      if (!pgrid_ok(H)) return tm.rank == 0 ? exact_row() : -1;
+      tm.push(sm.misc, 1, rp_pass_a<kBF16>(rc, H, eps, sm.hist, sm.cw, sm.red));
+      tm.sync();
+    }
   }
   // bin factors exp(-b/32), the bin masses summed over the members, their total S, and
   // the bin bstar holding the boundary (its prefix reaches p * S)
@@ -1549,11 +1626,16 @@ __device__ __noinline__ int32_t rwide_row(const RowCtx& rc, const RowSmem& sm, c
     for (int e = 0; e < per; ++e) {
       const int b = per * static_cast<int>(threadIdx.x) + e;
       unsigned long long c = 0, wb = 0;
-      for (int r = 0; r < tm.C; ++r) {
-        const uint32_t* hr = tm.remote(sm.hist, r);
-        const unsigned long long x = tm.remote(sm.cw, r)[b];
-        c += static_cast<unsigned long long>(hr[b]) + (static_cast<unsigned long long>(hr[kRPBins + b]) << 12);
-        wb = x > wb ? x : wb;
+      if (from_rec) {
+        c = __ldcg(rec->sums + b);
+        wb = __ldcg(rec->ub + b);
+      } else {
+        for (int r = 0; r < tm.C; ++r) {
+          const uint32_t* hr = tm.remote(sm.hist, r);
+          const unsigned long long x = tm.remote(sm.cw, r)[b];
+          c += static_cast<unsigned long long>(hr[b]) + (static_cast<unsigned long long>(hr[kRPBins + b]) << 12);
+          wb = x > wb ? x : wb;
+        }
       }
       ubest[e] = wb;
       m[e] = static_cast<double>(c) * 5.9604644775390625e-8 * static_cast<double>(pfac(b));
@@ -1616,6 +1698,7 @@ __device__ __noinline__ int32_t rwide_row(const RowCtx& rc, const RowSmem& sm, c
     rblock_max2(rb, dummy, sm.red);
   }
   tm.sync();  // every member is done reading the histograms, the per-bin words and the slots
+  if (from_rec) prec_clear(*rec, tm);
 
   // pass B over this CTA's part
   const uint32_t wcnt = rp_pass_b<kBF16>(rc, H, bstar, sm.cw);
@@ -1857,7 +1940,8 @@ __device__ __forceinline__ bool row_is_wide(const Params& P, int64_t row) { retu
 // The work units of the launch: every wide row (top-p-only or keep-all) is one unit for
 // all C CTAs of a cluster; top-k and one-element rows come C to a unit, one per CTA, unless
 // every row fits a cluster of its own (then rank 0 takes it and the rows spread over more
-// SMs).  Units go round-robin over the clusters.  Writes this CTA's items in unit order
+// SMs).  Units go round-robin over the clusters: the wide units first, or, when a pre-pass
+// runs alongside (its rows wait for it), last.  Writes this CTA's items in unit order
 // (>= 0: a row of its own, -1: nothing in that unit, <= -2: wide row -(item + 2)) and
 // returns their count, or -1 when they do not fit kRMaxItems.
 __device__ int rbuild_items(const Params& P, int C, int rank, int cluster, int nclusters, int32_t* items,
@@ -1867,7 +1951,9 @@ __device__ int rbuild_items(const Params& P, int C, int rank, int cluster, int n
   rblock_sum_max2(nwide, dummy0, dummy1, red);
   const int64_t nk = P.B - static_cast<int64_t>(nwide);
   const int per = P.B <= nclusters ? 1 : C;  // top-k rows per unit
-  const int64_t units = static_cast<int64_t>(nwide) + (nk + per - 1) / per;
+  const int64_t kunits = (nk + per - 1) / per;
+  const int64_t units = static_cast<int64_t>(nwide) + kunits;
+  const bool wide_last = P.pre != nullptr;
   const int64_t mine = units > cluster ? (units - 1 - cluster) / nclusters + 1 : 0;
   if ((units + nclusters - 1) / nclusters > kRMaxItems) return -1;  // the same answer in every CTA
   for (int i = threadIdx.x; i < mine; i += kRT) items[i] = -1;
@@ -1884,11 +1970,11 @@ __device__ int rbuild_items(const Params& P, int C, int rank, int cluster, int n
     if (valid) {
       int64_t unit, slot;
       if (wide) {
-        unit = static_cast<int64_t>(wbase + (ex >> 32));
+        unit = static_cast<int64_t>(wbase + (ex >> 32)) + (wide_last ? kunits : 0);
         slot = rank;
       } else {
         const int64_t ko = static_cast<int64_t>(kbase + (ex & 0xFFFFFFFFull));
-        unit = static_cast<int64_t>(nwide) + ko / per;
+        unit = (wide_last ? 0 : static_cast<int64_t>(nwide)) + ko / per;
         slot = ko % per;
       }
       if (unit % nclusters == cluster && slot == rank)
@@ -1899,6 +1985,146 @@ __device__ int rbuild_items(const Params& P, int C, int rank, int cluster, int n
   }
   __syncthreads();
   return static_cast<int>(mine);
+}
+
+// The parameters of a row and its context for part `part` of `nparts` (a team member's
+// share of the vectors); sets the seen bits of the row in the bitmap (which is clear).
+struct RowFlags {
+  int32_t k;
+  float p;
+  bool pen_on, single, topp_on;
+  int32_t b0, b1;  // the row's seen ids
+};
+template <bool kBF16>
+__device__ __forceinline__ RowFlags row_setup(const Params& P, int64_t row, const RowSmem& sm, int part, int nparts,
+                                              RowCtx* rcp) {
+  constexpr int G = kBF16 ? 8 : 4;
+  const size_t esize = kBF16 ? 2 : 4;
+  const int V = static_cast<int>(P.V);
+  RowFlags f;
+  f.k = P.top_k[row];
+  f.p = P.top_p[row];
+  const float T = P.temperature[row];
+  const bool greedyT = !(T > 0.0f) || isinf(T);
+  f.pen_on = P.seen_indptr && P.seen_ids && P.penalty && (P.penalty[row] > 0.0f);
+  const bool topk_on = f.k >= 1 && static_cast<int64_t>(f.k) <= (P.V < kTopKMax ? P.V : kTopKMax);
+  const bool p_nan = isnan(f.p);
+  f.single = greedyT || (!p_nan && f.p <= 0.0f) || (topk_on && f.k == 1);
+  f.topp_on = !f.single && !p_nan && f.p > 0.0f && f.p < 1.0f;
+  RowCtx& rc = *rcp;
+  rc.x = reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(P.logits) + row * P.V * esize);
+  rc.q = P.q + row * P.V;
+  rc.out = P.need_logits ? P.out_filtered + row * P.V : nullptr;
+  rc.V = V;
+  rc.nv = V / G;
+  rc.g0 = static_cast<int>(static_cast<int64_t>(rc.nv) * part / nparts);
+  rc.g1 = static_cast<int>(static_cast<int64_t>(rc.nv) * (part + 1) / nparts);
+  rc.bitmap = sm.bitmap;
+  rc.pen_on = f.pen_on;
+  rc.pen = f.pen_on ? P.penalty[row] : 1.0f;
+  rc.T = T;
+  rc.div = make_divisor(greedyT ? 1.0f : T);
+  rc.identity = greedyT;
+  __syncthreads();  // the bitmap of the previous row is clear
+  f.b0 = 0;
+  f.b1 = 0;
+  if (f.pen_on) {
+    f.b0 = P.seen_indptr[row];
+    f.b1 = P.seen_indptr[row + 1];
+    for (int32_t t = f.b0 + static_cast<int32_t>(threadIdx.x); t < f.b1; t += kRT) {
+      const int32_t id = P.seen_ids[t];
+      if (id >= 0 && id < V) atomicOr(&sm.bitmap[id >> 5], 1u << (id & 31));
+    }
+  }
+  __syncthreads();
+  return f;
+}
+// Clears the row's seen bits again.
+__device__ __forceinline__ void row_teardown(const Params& P, int64_t row, const RowFlags& f, const RowSmem& sm) {
+  if (!f.pen_on) return;
+  const int V = static_cast<int>(P.V);
+  for (int32_t t = f.b0 + static_cast<int32_t>(threadIdx.x); t < f.b1; t += kRT) {
+    const int32_t id = P.seen_ids[t];
+    if (id >= 0 && id < V) sm.bitmap[id >> 5] = 0u;
+  }
+}
+
+// The pre-pass: pass A of every top-p-only row with a record, each row cut into chunks
+// spread over the grid (as many as the grid holds, up to kPreMaxChunks).  Every CTA of a
+// row samples the same elements for H; each runs pass A over its chunk in shared memory
+// and merges the bin sums and race words into the row's record with global atomics.
+template <bool kBF16>
+__global__ void __launch_bounds__(kRT, 2) kps_prepass_kernel(const Params P) {
+  extern __shared__ __align__(16) unsigned char r_smem[];
+  const RLayout lay = make_rlayout(P.V);
+  RowSmem sm;
+  sm.bitmap = reinterpret_cast<uint32_t*>(r_smem + lay.bitmap);
+  sm.cw = reinterpret_cast<unsigned long long*>(r_smem + lay.cw);
+  sm.hist = reinterpret_cast<uint32_t*>(r_smem + lay.hist);
+  sm.wbuf = reinterpret_cast<unsigned long long*>(r_smem + lay.wbuf);
+  sm.red = reinterpret_cast<unsigned long long*>(r_smem + lay.red);
+  sm.misc = reinterpret_cast<unsigned long long*>(r_smem + lay.misc);
+  // the row kernel may start now: its rows that need a record wait for this grid to end
+  asm volatile("griddepcontrol.launch_dependents;");
+  const int V = static_cast<int>(P.V);
+  for (int w = threadIdx.x; w < (V + 31) / 32; w += kRT) sm.bitmap[w] = 0u;
+  unsigned long long cnt = 0;
+  for (int64_t r = threadIdx.x; r < P.B; r += kRT) cnt += row_prepass(P, r) ? 1ull : 0ull;
+  cnt = rblock_sum_u64(cnt, sm.red);
+  const int np = static_cast<int>(cnt < static_cast<unsigned long long>(P.pre_rows) ? cnt : P.pre_rows);
+  if (np == 0) return;
+  // CTAs for the pre-pass: what the other rows leave of the grid, and at least half of it
+  // (the CTAs past the units leave at once, making room for the row kernel)
+  const int64_t others = P.B - static_cast<int64_t>(cnt);
+  const int64_t half = static_cast<int64_t>(gridDim.x) / 2;
+  const int64_t slots = static_cast<int64_t>(gridDim.x) - others > half ? static_cast<int64_t>(gridDim.x) - others : half;
+  int nch = static_cast<int>(slots / np);
+  nch = nch < 1 ? 1 : (nch > kPreMaxChunks ? kPreMaxChunks : nch);
+  const int units = np * nch;
+  int64_t& s_row = *reinterpret_cast<int64_t*>(sm.misc + kMFound);
+  for (int u = static_cast<int>(blockIdx.x); u < units; u += static_cast<int>(gridDim.x)) {
+    const int j = u / nch, c = u - (u / nch) * nch;
+    // the j-th row with row_prepass
+    if (threadIdx.x == 0) s_row = -1;
+    unsigned long long run = 0;
+    for (int64_t b0 = 0; b0 < P.B; b0 += kRT) {
+      const int64_t r = b0 + threadIdx.x;
+      const unsigned long long v = (r < P.B && row_prepass(P, r)) ? 1ull : 0ull;
+      unsigned long long tot;
+      const unsigned long long ex = rblock_excl_scan_u64(v, &tot, sm.red);
+      if (v && run + ex == static_cast<unsigned long long>(j)) s_row = r;
+      run += tot;
+      if (run > static_cast<unsigned long long>(j)) break;  // the same for every thread
+    }
+    __syncthreads();
+    const int64_t row = s_row;
+    RowCtx rc;
+    const RowFlags f = row_setup<kBF16>(P, row, sm, c, nch, &rc);
+    RowCtx whole = rc;
+    whole.g0 = 0;
+    whole.g1 = rc.nv;
+    uint32_t* samp = reinterpret_cast<uint32_t*>(sm.wbuf);
+    rsample_load<kBF16>(whole, samp);
+    unsigned long long a = 0, b = 0;
+    for (int i = threadIdx.x; i < kRSamp; i += kRT) a = samp[i] > a ? samp[i] : a;
+    rblock_max2(a, b, sm.red);
+    const float H = pgrid_up(__fadd_rn(kfloat(static_cast<uint32_t>(a)), kRHeadroom));
+    const PRec rec = prec_at(P, j);
+    if (c == 0 && threadIdx.x == 0) *rec.H = __float_as_uint(H);
+    if (pgrid_ok(H)) {
+      const unsigned long long kmax = rp_pass_a<kBF16>(rc, H, P.eps, sm.hist, sm.cw, sm.red);
+      for (int bb = threadIdx.x; bb < kRPBins; bb += kRT) {
+        const unsigned long long sb =
+            static_cast<unsigned long long>(sm.hist[bb]) + (static_cast<unsigned long long>(sm.hist[kRPBins + bb]) << 12);
+        if (sb) atomicAdd(rec.sums + bb, sb);
+        const unsigned long long wb = sm.cw[bb];
+        if (wb) atomicMax(rec.ub + bb, wb);
+      }
+      if (threadIdx.x == 0) atomicMax(rec.M, kmax);
+    }
+    __syncthreads();
+    row_teardown(P, row, f, sm);
+  }
 }
 
 template <bool kBF16>
@@ -1913,9 +2139,7 @@ __global__ void __launch_bounds__(kRT, 2) kps_row_kernel(const Params P) {
   sm.red = reinterpret_cast<unsigned long long*>(r_smem + lay.red);
   sm.misc = reinterpret_cast<unsigned long long*>(r_smem + lay.misc);
   int32_t* items = reinterpret_cast<int32_t*>(r_smem + lay.items);
-  constexpr int G = kBF16 ? 8 : 4;
   const int V = static_cast<int>(P.V);
-  const size_t esize = kBF16 ? 2 : 4;
   for (int w = threadIdx.x; w < (V + 31) / 32; w += kRT) sm.bitmap[w] = 0u;
 
   cg::cluster_group cl = cg::this_cluster();
@@ -1945,58 +2169,27 @@ __global__ void __launch_bounds__(kRT, 2) kps_row_kernel(const Params P) {
       wide = row_is_wide(P, row);
     }
     const Team& tm = wide ? team : alone;
-    const int32_t k = P.top_k[row];
-    const float p = P.top_p[row];
-    const float T = P.temperature[row];
-    const bool greedyT = !(T > 0.0f) || isinf(T);
-    const bool pen_on = P.seen_indptr && P.seen_ids && P.penalty && (P.penalty[row] > 0.0f);
-    const bool topk_on = k >= 1 && static_cast<int64_t>(k) <= (P.V < kTopKMax ? P.V : kTopKMax);
-    const bool p_nan = isnan(p);
-    const bool single = greedyT || (!p_nan && p <= 0.0f) || (topk_on && k == 1);
-    const bool topp_on = !single && !p_nan && p > 0.0f && p < 1.0f;
-
     RowCtx rc;
-    rc.x = reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(P.logits) + row * P.V * esize);
-    rc.q = P.q + row * P.V;
-    rc.out = P.need_logits ? P.out_filtered + row * P.V : nullptr;
-    rc.V = V;
-    rc.nv = V / G;
-    rc.g0 = static_cast<int>(static_cast<int64_t>(rc.nv) * tm.rank / tm.C);
-    rc.g1 = static_cast<int>(static_cast<int64_t>(rc.nv) * (tm.rank + 1) / tm.C);
-    rc.bitmap = sm.bitmap;
-    rc.pen_on = pen_on;
-    rc.pen = pen_on ? P.penalty[row] : 1.0f;
-    rc.T = T;
-    rc.div = make_divisor(greedyT ? 1.0f : T);
-    rc.identity = greedyT;
-
-    __syncthreads();  // the bitmap of the previous row is clear
-    int32_t b0 = 0, b1 = 0;
-    if (pen_on) {
-      b0 = P.seen_indptr[row];
-      b1 = P.seen_indptr[row + 1];
-      for (int32_t t = b0 + static_cast<int32_t>(threadIdx.x); t < b1; t += kRT) {
-        const int32_t id = P.seen_ids[t];
-        if (id >= 0 && id < V) atomicOr(&sm.bitmap[id >> 5], 1u << (id & 31));
-      }
-    }
-    __syncthreads();
-
+    const RowFlags f = row_setup<kBF16>(P, row, sm, tm.rank, tm.C, &rc);
     int32_t chosen;
     if (!wide) {
-      chosen = rk_row<kBF16>(rc, sm, single ? 1u : static_cast<uint32_t>(k), single, topp_on, p, P.eps,
+      chosen = rk_row<kBF16>(rc, sm, f.single ? 1u : static_cast<uint32_t>(f.k), f.single, f.topp_on, f.p, P.eps,
                              P.exact != 0);
     } else {
-      chosen = rwide_row<kBF16>(rc, sm, tm, topp_on, p, P.eps, P.exact != 0);
+      PRec rec;
+      bool has_rec = false;
+      if (P.pre && f.topp_on && row_prepass(P, row)) {
+        const int j = prepass_ordinal(P, row, sm.red);
+        if (j < P.pre_rows) {
+          rec = prec_at(P, j);
+          has_rec = true;
+        }
+      }
+      chosen = rwide_row<kBF16>(rc, sm, tm, f.topp_on, f.p, P.eps, P.exact != 0, has_rec ? &rec : nullptr);
     }
     if (threadIdx.x == 0 && chosen >= 0) P.out_idx[row] = chosen;
     __syncthreads();
-    if (pen_on) {
-      for (int32_t t = b0 + static_cast<int32_t>(threadIdx.x); t < b1; t += kRT) {
-        const int32_t id = P.seen_ids[t];
-        if (id >= 0 && id < V) sm.bitmap[id >> 5] = 0u;
-      }
-    }
+    row_teardown(P, row, f, sm);
   }
   // members of a cluster leave together: no CTA exits while another may still read its
   // shared memory

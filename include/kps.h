@@ -164,6 +164,11 @@ int kps_get_kernel_policy(void);
  * 2 = the row kernel (kps_row_kernel), 0 = none yet. */
 int kps_last_kernel(void);
 
+/* Kernels the most recent kps_sample call of the calling host thread that
+ * launched any queued: 1, or 2 when the row kernel was preceded by its
+ * pre-pass over the top-p-only rows (kps_prepass_kernel); 0 = none yet. */
+int kps_last_launch_count(void);
+
 /* Static description of a status code. */
 const char* kps_status_string(kps_status s);
 

@@ -32,7 +32,12 @@ def test_exports_every_declared_function(lib):
 
 
 def test_workspace_size(lib):
-    assert lib.kps_workspace_size(256, 151936, 0) >= 4
+    # the status word, plus one 32896-byte pre-pass record per row (top-p-only rows of a
+    # vocabulary past 4096) for up to 1024 rows
+    assert lib.kps_workspace_size(256, 151936, 0) == 256 + 256 * 32896
+    assert lib.kps_workspace_size(4000, 151936, 1) == 256 + 1024 * 32896
+    assert lib.kps_workspace_size(64, 4096, 0) == 256
+    assert lib.kps_workspace_size(0, 151936, 0) == 256
     assert lib.kps_workspace_size(-1, 10, 0) == 0
     assert lib.kps_workspace_size(1, 0, 0) == 0
     assert lib.kps_workspace_size(1, 10, 7) == 0

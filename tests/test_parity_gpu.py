@@ -145,3 +145,71 @@ def test_batch_sizes_and_row_walk(B, kernel):
     ref = oracle.sample(inp)
     gi, gf = run_gpu(inp)
     compare(inp, ref, gi, gf, f"B={B} [{kernel}]")
+
+
+PREC_BYTES = 32896  # one pre-pass record (bin sums, race words, the maximum and H)
+
+
+@pytest.mark.parametrize("name", ["batch256_penalty", "flat_nucleus"])
+@pytest.mark.parametrize("records", [0, 3])
+def test_row_kernel_with_few_pre_pass_records(name, records):
+    """A workspace with room for no (or only 3) pre-pass records: the top-p-only rows beyond
+    them run their own pass A inside the row kernel.  Same results as the oracle."""
+    import torch
+    import decode_token_sampling_gb300 as kps
+    kps.set_kernel_policy(kps.KERNEL_ROW)
+    try:
+        inp = make_workload(name)
+        ref = oracle.sample(inp)
+        ws = torch.zeros(256 + records * PREC_BYTES, dtype=torch.uint8, device="cuda:0")
+        gi, gf = run_gpu(inp, workspace=ws)
+        compare(inp, ref, gi, gf, f"{name} [{records} records]")
+        assert kps.last_device_status(ws) == 0
+        assert int(ws[256:].count_nonzero().item()) == 0
+    finally:
+        kps.set_kernel_policy(kps.KERNEL_AUTO)
+
+
+@pytest.mark.parametrize("name", ["batch256_penalty", "flat_nucleus"])
+def test_pre_pass_leaves_its_records_zeroed(name):
+    """The row kernel clears every pre-pass record it reads: several calls on one workspace
+    give the oracle's results and leave everything past the status word zero."""
+    import torch
+    import decode_token_sampling_gb300 as kps
+    kps.set_kernel_policy(kps.KERNEL_ROW)
+    try:
+        inp = make_workload(name)
+        ref = oracle.sample(inp)
+        ws = kps.new_workspace(inp.B, inp.V, torch.float32, "cuda:0")
+        assert ws.numel() >= 256 + PREC_BYTES * min(inp.B, 1024)
+        for _ in range(3):
+            gi, gf = run_gpu(inp, workspace=ws)
+            compare(inp, ref, gi, gf, f"{name} [reused workspace]")
+        assert kps.last_device_status(ws) == 0
+        assert int(ws[256:].count_nonzero().item()) == 0
+    finally:
+        kps.set_kernel_policy(kps.KERNEL_AUTO)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_pre_pass_with_many_top_p_rows(dtype):
+    """More rows than the grid has clusters, most of them top-p-only (so their pass A runs in
+    the pre-pass, several chunks to a row), with penalties, a vocabulary that is no multiple
+    of a tile (rows still start on 16-byte boundaries, as the row kernel needs) and some
+    top-k rows between them."""
+    import torch
+    import decode_token_sampling_gb300 as kps
+    kps.set_kernel_policy(kps.KERNEL_ROW)
+    try:
+        inp = make_random(400, 12296, seed=41, dtype=dtype, k_range=(1, 64), k_skip_frac=0.8,
+                          p_range=(0.3, 0.999), penalty=1.3, n_seen=40)
+        ref = oracle.sample(inp)
+        ws = kps.new_workspace(inp.B, inp.V, torch.bfloat16 if dtype == "bf16" else torch.float32, "cuda:0")
+        for _ in range(2):
+            gi, gf = run_gpu(inp, workspace=ws)
+            compare(inp, ref, gi, gf, f"many top-p rows {dtype}")
+        assert kps.last_launch_count() == 2
+        assert kps.last_device_status(ws) == 0
+        assert int(ws[256:].count_nonzero().item()) == 0
+    finally:
+        kps.set_kernel_policy(kps.KERNEL_AUTO)
