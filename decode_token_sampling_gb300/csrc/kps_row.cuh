@@ -53,7 +53,7 @@ constexpr int kRMaxItems = 256;        // work units one CTA may own in one laun
 constexpr int kRMaxTeam = 4;           // CTAs that may share one row (the cluster size)
 
 struct RLayout {
-  size_t bitmap, cw, hist, wbuf, red, misc, items, total;
+  size_t bitmap, cw, hist, wbuf, red, misc, items, ords, total;
 };
 
 __host__ __device__ inline RLayout make_rlayout(int64_t V) {
@@ -66,6 +66,7 @@ __host__ __device__ inline RLayout make_rlayout(int64_t V) {
   L.red = off;    off += 64 * 8;
   L.misc = off;   off += 64 * 8;
   L.items = off;  off += size_t(kRMaxItems) * 4;
+  L.ords = off;   off += size_t(kRMaxItems) * 4;  // pre-pass record of each item (-1: none)
   L.total = off;
   return L;
 }
@@ -1252,12 +1253,17 @@ __device__ __forceinline__ float pgrid_up(float h) {
 }
 __device__ __forceinline__ bool pgrid_ok(float h) { return fabsf(h) < 262144.0f; }  // false for NaN, inf
 
-// The bin factor exp(-b/32), to about 2^-22 relative: the exponent is split in double
-// into an integer power of two and a fraction, so the error does not grow with b.
+// The bin factor exp(-b/32), to about 2^-22 relative: its base-2 exponent b log2(e) / 32
+// is split into an integer and a fraction with log2(e) / 32 carried as an 11-bit head
+// (whose product with b < 2^11 is exact) plus a tail, so the error does not grow with b.
 __device__ __forceinline__ float pfac(int b) {
-  const double z = static_cast<double>(b) * (1.4426950408889634074 / 32.0);
-  const double n = floor(z);
-  return __fmul_rn(rex2(-static_cast<float>(z - n)), __int_as_float((127 - static_cast<int>(n)) << 23));
+  constexpr float kHead = 0.045074462890625f;        // log2(e) / 32 to 12 bits (1477 / 2^15)
+  constexpr float kTail = 9.757137155105844e-06f;     // log2(e) / 32 - kHead
+  const float fb = static_cast<float>(b);
+  const float zh = __fmul_rn(fb, kHead);             // exact
+  const float n = floorf(zh);
+  const float frac = __fmaf_rn(fb, kTail, __fsub_rn(zh, n));  // in [0, 1.02)
+  return __fmul_rn(rex2(-frac), __int_as_float((127 - static_cast<int>(n)) << 23));
 }
 
 // The weight of y against the reference H (on the grid, H >= y): its bin
@@ -1945,7 +1951,7 @@ __device__ __forceinline__ bool row_is_wide(const Params& P, int64_t row) { retu
 // (>= 0: a row of its own, -1: nothing in that unit, <= -2: wide row -(item + 2)) and
 // returns their count, or -1 when they do not fit kRMaxItems.
 __device__ int rbuild_items(const Params& P, int C, int rank, int cluster, int nclusters, int32_t* items,
-                            unsigned long long* red) {
+                            int32_t* ords, unsigned long long* red) {
   unsigned long long nwide = 0, dummy0 = 0, dummy1 = 0;
   for (int64_t r = threadIdx.x; r < P.B; r += kRT) nwide += row_is_wide(P, r) ? 1ull : 0ull;
   rblock_sum_max2(nwide, dummy0, dummy1, red);
@@ -1956,9 +1962,12 @@ __device__ int rbuild_items(const Params& P, int C, int rank, int cluster, int n
   const bool wide_last = P.pre != nullptr;
   const int64_t mine = units > cluster ? (units - 1 - cluster) / nclusters + 1 : 0;
   if ((units + nclusters - 1) / nclusters > kRMaxItems) return -1;  // the same answer in every CTA
-  for (int i = threadIdx.x; i < mine; i += kRT) items[i] = -1;
+  for (int i = threadIdx.x; i < mine; i += kRT) {
+    items[i] = -1;
+    ords[i] = -1;
+  }
   __syncthreads();
-  unsigned long long wbase = 0, kbase = 0;
+  unsigned long long wbase = 0, kbase = 0, pbase = 0;
   for (int64_t base = 0; base < P.B; base += kRT) {
     const int64_t r = base + threadIdx.x;
     const bool valid = r < P.B;
@@ -1967,6 +1976,10 @@ __device__ int rbuild_items(const Params& P, int C, int rank, int cluster, int n
     const unsigned long long v = valid ? (wide ? (1ull << 32) : 1ull) : 0ull;
     unsigned long long tot;
     const unsigned long long ex = rblock_excl_scan_u64(v, &tot, red);
+    // ordinals among the pre-pass rows (only with records)
+    const bool pre = P.pre != nullptr && valid && row_prepass(P, r);
+    unsigned long long ptot = 0, pex = 0;
+    if (P.pre != nullptr) pex = rblock_excl_scan_u64(pre ? 1ull : 0ull, &ptot, red);
     if (valid) {
       int64_t unit, slot;
       if (wide) {
@@ -1977,11 +1990,15 @@ __device__ int rbuild_items(const Params& P, int C, int rank, int cluster, int n
         unit = (wide_last ? 0 : static_cast<int64_t>(nwide)) + ko / per;
         slot = ko % per;
       }
-      if (unit % nclusters == cluster && slot == rank)
+      if (unit % nclusters == cluster && slot == rank) {
         items[unit / nclusters] = wide ? static_cast<int32_t>(-(r + 2)) : static_cast<int32_t>(r);
+        const unsigned long long po = pbase + pex;
+        if (pre && po < static_cast<unsigned long long>(P.pre_rows)) ords[unit / nclusters] = static_cast<int32_t>(po);
+      }
     }
     wbase += tot >> 32;
     kbase += tot & 0xFFFFFFFFull;
+    pbase += ptot;
   }
   __syncthreads();
   return static_cast<int>(mine);
@@ -2073,12 +2090,8 @@ __global__ void __launch_bounds__(kRT, 2) kps_prepass_kernel(const Params P) {
   cnt = rblock_sum_u64(cnt, sm.red);
   const int np = static_cast<int>(cnt < static_cast<unsigned long long>(P.pre_rows) ? cnt : P.pre_rows);
   if (np == 0) return;
-  // CTAs for the pre-pass: what the other rows leave of the grid, and at least half of it
-  // (the CTAs past the units leave at once, making room for the row kernel)
-  const int64_t others = P.B - static_cast<int64_t>(cnt);
-  const int64_t half = static_cast<int64_t>(gridDim.x) / 2;
-  const int64_t slots = static_cast<int64_t>(gridDim.x) - others > half ? static_cast<int64_t>(gridDim.x) - others : half;
-  int nch = static_cast<int>(slots / np);
+  // the whole grid (CTAs past the units leave at once, making room for the row kernel)
+  int nch = static_cast<int>(gridDim.x) / np;
   nch = nch < 1 ? 1 : (nch > kPreMaxChunks ? kPreMaxChunks : nch);
   const int units = np * nch;
   int64_t& s_row = *reinterpret_cast<int64_t*>(sm.misc + kMFound);
@@ -2139,6 +2152,7 @@ __global__ void __launch_bounds__(kRT, 2) kps_row_kernel(const Params P) {
   sm.red = reinterpret_cast<unsigned long long*>(r_smem + lay.red);
   sm.misc = reinterpret_cast<unsigned long long*>(r_smem + lay.misc);
   int32_t* items = reinterpret_cast<int32_t*>(r_smem + lay.items);
+  int32_t* ords = reinterpret_cast<int32_t*>(r_smem + lay.ords);
   const int V = static_cast<int>(P.V);
   for (int w = threadIdx.x; w < (V + 31) / 32; w += kRT) sm.bitmap[w] = 0u;
 
@@ -2147,7 +2161,7 @@ __global__ void __launch_bounds__(kRT, 2) kps_row_kernel(const Params P) {
   const int rank = static_cast<int>(cl.block_rank());
   const int cluster = static_cast<int>(blockIdx.x) / C;
   const int nclusters = static_cast<int>(gridDim.x) / C;
-  int nitems = rbuild_items(P, C, rank, cluster, nclusters, items, sm.red);
+  int nitems = rbuild_items(P, C, rank, cluster, nclusters, items, ords, sm.red);
   const bool shared_rows = nitems >= 0;
   if (!shared_rows) {
     // too many units for the item list: every CTA takes rows on its own, round-robin
@@ -2159,11 +2173,13 @@ __global__ void __launch_bounds__(kRT, 2) kps_row_kernel(const Params P) {
   for (int it = 0; it < nitems; ++it) {
     int64_t row;
     bool wide;
+    int32_t ord = -1;  // the row's pre-pass record
     if (shared_rows) {
       const int32_t item = items[it];
       if (item == -1) continue;
       wide = item <= -2;
       row = wide ? static_cast<int64_t>(-(item + 2)) : static_cast<int64_t>(item);
+      ord = ords[it];
     } else {
       row = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(it) * gridDim.x;
       wide = row_is_wide(P, row);
@@ -2177,15 +2193,12 @@ __global__ void __launch_bounds__(kRT, 2) kps_row_kernel(const Params P) {
                              P.exact != 0);
     } else {
       PRec rec;
-      bool has_rec = false;
-      if (P.pre && f.topp_on && row_prepass(P, row)) {
+      if (!shared_rows && P.pre && row_prepass(P, row)) {
         const int j = prepass_ordinal(P, row, sm.red);
-        if (j < P.pre_rows) {
-          rec = prec_at(P, j);
-          has_rec = true;
-        }
+        ord = j < P.pre_rows ? j : -1;
       }
-      chosen = rwide_row<kBF16>(rc, sm, tm, f.topp_on, f.p, P.eps, P.exact != 0, has_rec ? &rec : nullptr);
+      if (ord >= 0) rec = prec_at(P, ord);
+      chosen = rwide_row<kBF16>(rc, sm, tm, f.topp_on, f.p, P.eps, P.exact != 0, ord >= 0 ? &rec : nullptr);
     }
     if (threadIdx.x == 0 && chosen >= 0) P.out_idx[row] = chosen;
     __syncthreads();
