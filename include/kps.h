@@ -67,10 +67,17 @@ typedef enum {
   KPS_ERR_TIMEOUT = 5       /* device side: a bounded wait ran out             */
 } kps_status;
 
-/* Bytes of device workspace kps_sample needs for a [B, V] call of dtype dt
- * (256-byte aligned start required).  The workspace holds the device status
- * word; zero it once before first use (kps_last_device_status also clears
- * it).  Returns 0 for invalid sizes. */
+/* Bytes of device workspace for the fastest schedule of a [B, V] call of
+ * dtype dt (256-byte aligned start required).  The first 256 bytes hold the
+ * device status word.  For V > 4096 one 32896-byte record per row follows
+ * (min(B, 1024) records): the pre-pass of the top-p-only rows merges their
+ * bin sums and race words there, and the row kernel reads and clears them.
+ * kps_sample accepts any workspace of at least 256 bytes; rows beyond the
+ * records it holds run their whole selection inside the row kernel instead.
+ * Zero the workspace once before its first use: every call leaves the
+ * records zeroed again (the status word aside, which kps_last_device_status
+ * reads and clears).  One call at a time may use a workspace.  Returns 0 for
+ * invalid sizes. */
 size_t kps_workspace_size(int64_t B, int64_t V, kps_dtype dt);
 
 /* Largest vocabulary size kps_sample accepts for dtype dt on the current
@@ -96,8 +103,9 @@ int64_t kps_max_vocab(kps_dtype dt);
  *   need_logits   non-zero: write out_filtered.
  *   out_idx       [B] int64 chosen token per row.
  *   out_filtered  [B, V] fp32; required iff need_logits.
- *   workspace     device buffer of at least kps_workspace_size(B, V, dt)
- *                 bytes, 256-byte aligned.
+ *   workspace     device buffer, 256-byte aligned, of at least 256 bytes;
+ *                 kps_workspace_size(B, V, dt) bytes for the fastest
+ *                 schedule.  Zeroed before its first use (see above).
  *   stream        CUDA stream the work is queued on (0 = legacy default).
  *
  * B == 0 is a valid no-op.  Returns KPS_OK once the work is queued.
@@ -119,15 +127,14 @@ kps_status kps_last_device_status(void* workspace, cudaStream_t stream, int* out
  * that owns all device memory and forbids outside allocations, a real-time
  * path where allocation latency or failure is not acceptable, or code that
  * runs under a memory budget it does not control.  This entry point needs no
- * workspace: its scratch (the device status word) lives in a fixed array
- * inside the library, 4096 bytes, held on every GPU that loads the library
- * until the process exits.  It allocates nothing and calls no allocating
+ * workspace: its scratch (a 256-byte workspace: the device status word)
+ * lives in a fixed array inside the library, 4096 bytes, held on every GPU
+ * that loads the library until the process exits.  It therefore never runs
+ * the pre-pass of the top-p-only rows.  It allocates nothing and calls no allocating
  * routine; the caller still passes inputs and outputs as for kps_sample.
  * (The method's pages have no counterpart to this entry point.)
  *
  *   - Arguments, results and math are exactly those of kps_sample.
- *   - Calls whose workspace would exceed the 4096-byte scratch are rejected
- *     with KPS_ERR_UNSUPPORTED before anything is launched.
  *   - The first call on each device looks up the scratch array's device
  *     address with that device current (and sets kernel attributes); make
  *     that first call before capturing the stream into a CUDA graph.
@@ -161,7 +168,8 @@ int kps_get_kernel_policy(void);
 
 /* Which kernel the most recent kps_sample call of the calling host thread
  * that launched one used: 1 = the cluster kernel (kps_sample_kernel),
- * 2 = the row kernel (kps_row_kernel), 0 = none yet. */
+ * 2 = the row kernel (kps_row_kernel, possibly after its pre-pass
+ * kps_prepass_kernel), 0 = none yet. */
 int kps_last_kernel(void);
 
 /* Kernels the most recent kps_sample call of the calling host thread that
