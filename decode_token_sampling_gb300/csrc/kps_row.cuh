@@ -661,30 +661,41 @@ __device__ __forceinline__ int rbuf_gather(const unsigned long long* cw, int n, 
 
 // Keys of kRSamp transformed elements: 64 runs of 32 consecutive elements spread
 // evenly over the row (V > kRKeepAllV), one load per run and lane issued together.
+struct SampleLoads {
+  float x[kRRuns / kRW];
+  int idx[kRRuns / kRW];
+};
 template <bool kBF16>
-__device__ __forceinline__ void rsample_load(const RowCtx& rc, uint32_t* samp) {
+__device__ __forceinline__ void rsample_fetch(const RowCtx& rc, SampleLoads* sl) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  constexpr int per = kRRuns / kRW;
-  float x[per];
-  int idx[per];
 #pragma unroll
-  for (int u = 0; u < per; ++u) {
+  for (int u = 0; u < kRRuns / kRW; ++u) {
     const int j = warp + u * kRW;
-    idx[u] = static_cast<int>(static_cast<int64_t>(j) * (rc.V - 32) / (kRRuns - 1)) + lane;
+    sl->idx[u] = static_cast<int>(static_cast<int64_t>(j) * (rc.V - 32) / (kRRuns - 1)) + lane;
     if (kBF16) {
-      const unsigned short b = __ldg(reinterpret_cast<const unsigned short*>(rc.x) + idx[u]);
-      x[u] = __uint_as_float(static_cast<uint32_t>(b) << 16);
+      const unsigned short b = __ldg(reinterpret_cast<const unsigned short*>(rc.x) + sl->idx[u]);
+      sl->x[u] = __uint_as_float(static_cast<uint32_t>(b) << 16);
     } else {
-      x[u] = __ldg(reinterpret_cast<const float*>(rc.x) + idx[u]);
+      sl->x[u] = __ldg(reinterpret_cast<const float*>(rc.x) + sl->idx[u]);
     }
   }
+}
+// The sample's keys (the row's seen bits set), then a barrier.
+__device__ __forceinline__ void rsample_finish(const RowCtx& rc, const SampleLoads& sl, uint32_t* samp) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
-  for (int u = 0; u < per; ++u) {
+  for (int u = 0; u < kRRuns / kRW; ++u) {
     const int j = warp + u * kRW;
-    const bool seen = rc.pen_on && ((rc.bitmap[idx[u] >> 5] >> (idx[u] & 31)) & 1u);
-    samp[j * 32 + lane] = fkey(rtransform(x[u], seen, rc.pen, rc.div, rc.identity));
+    const bool seen = rc.pen_on && ((rc.bitmap[sl.idx[u] >> 5] >> (sl.idx[u] & 31)) & 1u);
+    samp[j * 32 + lane] = fkey(rtransform(sl.x[u], seen, rc.pen, rc.div, rc.identity));
   }
   __syncthreads();
+}
+template <bool kBF16>
+__device__ __forceinline__ void rsample_load(const RowCtx& rc, uint32_t* samp) {
+  SampleLoads sl;
+  rsample_fetch<kBF16>(rc, &sl);
+  rsample_finish(rc, sl, samp);
 }
 
 // The r-th largest sample key, rounded down to a multiple of 2^10 (two 11-bit digit
@@ -1007,7 +1018,7 @@ constexpr Thresh kKeepAll{1u, -1};  // kept_by(any real key) holds; empty slots 
 // Top-k and one-element rows; returns the chosen index.
 template <bool kBF16>
 __device__ __noinline__ int32_t rk_row(const RowCtx& rc, const RowSmem& sm, uint32_t keff, bool single, bool topp_on,
-                                       float p, float eps, bool exact) {
+                                       float p, float eps, bool exact, bool sampled) {
   uint32_t& s_cnt = *reinterpret_cast<uint32_t*>(sm.misc + kMCnt);
   uint32_t* segcnt = reinterpret_cast<uint32_t*>(sm.misc + kMSeg);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1018,7 +1029,10 @@ __device__ __noinline__ int32_t rk_row(const RowCtx& rc, const RowSmem& sm, uint
     tau_raw = __int_as_float(0x7fffffff);  // nothing passes: the exact select below takes over
   } else if (!keep_all) {
     uint32_t* samp = reinterpret_cast<uint32_t*>(sm.wbuf);
-    rsample_load<kBF16>(rc, samp);
+    if (!sampled) rsample_load<kBF16>(rc, samp);
+    // the streaming pass's first two rounds of loads, asked of L2 during the selection
+    for (int o = static_cast<int>(threadIdx.x) * 128; o < 2 * kRT * kRU * 16 && o < rc.nv * 16; o += kRT * 128)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(rc.x) + o));
     const int64_t want = (5 * static_cast<int64_t>(keff)) / 2 + 512;
     int64_t r = (want * kRSamp + rc.V - 1) / rc.V + 1;
     if (r > kRSamp) r = kRSamp;
@@ -1952,6 +1966,48 @@ __device__ __forceinline__ bool row_is_wide(const Params& P, int64_t row) { retu
 // returns their count, or -1 when they do not fit kRMaxItems.
 __device__ int rbuild_items(const Params& P, int C, int rank, int cluster, int nclusters, int32_t* items,
                             int32_t* ords, unsigned long long* red) {
+  if (P.B <= kRT) {
+    // one row per thread: its class read once, one scan of the packed counts
+    // (wide << 40 | pre-pass << 20 | top-k; B < 2^20)
+    const int64_t r = threadIdx.x;
+    const bool valid = r < P.B;
+    const bool wide = valid && row_is_wide(P, r);
+    const bool pre = P.pre != nullptr && valid && row_prepass(P, r);
+    const unsigned long long v =
+        valid ? (wide ? (1ull << 40) : 1ull) + (pre ? (1ull << 20) : 0ull) : 0ull;
+    unsigned long long tot;
+    const unsigned long long ex = rblock_excl_scan_u64(v, &tot, red);
+    const int64_t nwide = static_cast<int64_t>(tot >> 40), nk = static_cast<int64_t>(tot & 0xFFFFFull);
+    const int per = P.B <= nclusters ? 1 : C;  // top-k rows per unit
+    const int64_t kunits = (nk + per - 1) / per;
+    const int64_t units = nwide + kunits;
+    const bool wide_last = P.pre != nullptr;
+    const int64_t mine = units > cluster ? (units - 1 - cluster) / nclusters + 1 : 0;
+    if ((units + nclusters - 1) / nclusters > kRMaxItems) return -1;  // the same answer in every CTA
+    for (int i = threadIdx.x; i < mine; i += kRT) {
+      items[i] = -1;
+      ords[i] = -1;
+    }
+    __syncthreads();
+    if (valid) {
+      int64_t unit, slot;
+      if (wide) {
+        unit = static_cast<int64_t>(ex >> 40) + (wide_last ? kunits : 0);
+        slot = rank;
+      } else {
+        const int64_t ko = static_cast<int64_t>(ex & 0xFFFFFull);
+        unit = (wide_last ? 0 : nwide) + ko / per;
+        slot = ko % per;
+      }
+      if (unit % nclusters == cluster && slot == rank) {
+        items[unit / nclusters] = wide ? static_cast<int32_t>(-(r + 2)) : static_cast<int32_t>(r);
+        const unsigned long long po = (ex >> 20) & 0xFFFFFull;
+        if (pre && po < static_cast<unsigned long long>(P.pre_rows)) ords[unit / nclusters] = static_cast<int32_t>(po);
+      }
+    }
+    __syncthreads();
+    return static_cast<int>(mine);
+  }
   unsigned long long nwide = 0, dummy0 = 0, dummy1 = 0;
   for (int64_t r = threadIdx.x; r < P.B; r += kRT) nwide += row_is_wide(P, r) ? 1ull : 0ull;
   rblock_sum_max2(nwide, dummy0, dummy1, red);
@@ -2014,7 +2070,7 @@ struct RowFlags {
 };
 template <bool kBF16>
 __device__ __forceinline__ RowFlags row_setup(const Params& P, int64_t row, const RowSmem& sm, int part, int nparts,
-                                              RowCtx* rcp) {
+                                              RowCtx* rcp, bool sample = false) {
   constexpr int G = kBF16 ? 8 : 4;
   const size_t esize = kBF16 ? 2 : 4;
   const int V = static_cast<int>(P.V);
@@ -2042,6 +2098,10 @@ __device__ __forceinline__ RowFlags row_setup(const Params& P, int64_t row, cons
   rc.T = T;
   rc.div = make_divisor(greedyT ? 1.0f : T);
   rc.identity = greedyT;
+  // the sample of a top-k row (its threshold comes first): loads issued before the
+  // seen ids', transformed once the bitmap is built
+  SampleLoads sl;
+  if (sample) rsample_fetch<kBF16>(rc, &sl);
   __syncthreads();  // the bitmap of the previous row is clear
   f.b0 = 0;
   f.b1 = 0;
@@ -2054,6 +2114,7 @@ __device__ __forceinline__ RowFlags row_setup(const Params& P, int64_t row, cons
     }
   }
   __syncthreads();
+  if (sample) rsample_finish(rc, sl, reinterpret_cast<uint32_t*>(sm.wbuf));
   return f;
 }
 // Clears the row's seen bits again.
@@ -2186,11 +2247,12 @@ __global__ void __launch_bounds__(kRT, 2) kps_row_kernel(const Params P) {
     }
     const Team& tm = wide ? team : alone;
     RowCtx rc;
-    const RowFlags f = row_setup<kBF16>(P, row, sm, tm.rank, tm.C, &rc);
+    const bool sample = !wide && !P.exact && P.V > kRKeepAllV;
+    const RowFlags f = row_setup<kBF16>(P, row, sm, tm.rank, tm.C, &rc, sample);
     int32_t chosen;
     if (!wide) {
       chosen = rk_row<kBF16>(rc, sm, f.single ? 1u : static_cast<uint32_t>(f.k), f.single, f.topp_on, f.p, P.eps,
-                             P.exact != 0);
+                             P.exact != 0, sample);
     } else {
       PRec rec;
       if (!shared_rows && P.pre && row_prepass(P, row)) {
