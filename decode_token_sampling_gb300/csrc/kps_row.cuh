@@ -2173,12 +2173,9 @@ __global__ void __launch_bounds__(kRT, 2) kps_prepass_kernel(const Params P) {
     __syncthreads();
     const int64_t row = s_row;
     RowCtx rc;
-    const RowFlags f = row_setup<kBF16>(P, row, sm, c, nch, &rc);
-    RowCtx whole = rc;
-    whole.g0 = 0;
-    whole.g1 = rc.nv;
-    uint32_t* samp = reinterpret_cast<uint32_t*>(sm.wbuf);
-    rsample_load<kBF16>(whole, samp);
+    // the sample (the same elements in every chunk's CTA) is loaded alongside the seen ids
+    const RowFlags f = row_setup<kBF16>(P, row, sm, c, nch, &rc, true);
+    const uint32_t* samp = reinterpret_cast<const uint32_t*>(sm.wbuf);
     unsigned long long a = 0, b = 0;
     for (int i = threadIdx.x; i < kRSamp; i += kRT) a = samp[i] > a ? samp[i] : a;
     rblock_max2(a, b, sm.red);

@@ -213,3 +213,32 @@ def test_pre_pass_with_many_top_p_rows(dtype):
         assert int(ws[256:].count_nonzero().item()) == 0
     finally:
         kps.set_kernel_policy(kps.KERNEL_AUTO)
+
+
+@pytest.mark.parametrize("case", ["special", "spike", "huge"])
+def test_pre_pass_records_on_odd_rows(case):
+    """Top-p-only rows whose pre-pass record cannot be used as it stands: NaN and -inf logits
+    (special), a maximum the sample misses by far more than the headroom (spike: the row
+    redoes its pass A), and logits too large for the 1/32 grid (huge: the exact whole-row
+    selection).  Results match the oracle and every record is left zeroed."""
+    import torch
+    import decode_token_sampling_gb300 as kps
+    kps.set_kernel_policy(kps.KERNEL_ROW)
+    try:
+        inp = make_random(320, 8200, seed=77, k_range=(1, 64), k_skip_frac=0.7, p_range=(0.5, 0.99),
+                          special=(case == "special"))
+        if case == "spike":
+            for b in range(0, inp.B, 3):
+                inp.logits[b, (b * 977) % inp.V] = 60.0  # far above the rest, rarely in the sample
+        if case == "huge":
+            inp.logits[::2] *= 3.0e5
+        ref = oracle.sample(inp)
+        ws = kps.new_workspace(inp.B, inp.V, torch.float32, "cuda:0")
+        for _ in range(2):
+            gi, gf = run_gpu(inp, workspace=ws)
+            compare(inp, ref, gi, gf, f"odd rows {case}")
+        assert kps.last_launch_count() == 2
+        assert kps.last_device_status(ws) == 0
+        assert int(ws[256:].count_nonzero().item()) == 0
+    finally:
+        kps.set_kernel_policy(kps.KERNEL_AUTO)
