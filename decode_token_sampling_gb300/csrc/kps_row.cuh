@@ -637,24 +637,34 @@ __device__ __noinline__ Thresh rbuf_kth(const unsigned long long* cw, int n, uin
   return rbuf_radix(cw, n, k, hist, misc);
 }
 
-// Copies the nonzero entries of cw[0..n) kept by th to out[0..cap) (in no particular
-// order); returns their count, at most cap.
+// Copies the nonzero entries of cw[0..n) kept by th to out[0..cap), in buffer order;
+// returns their count, at most cap.  Positions come from one block-wide scan (a shared
+// counter would serialise one atomic per warp and round).
 __device__ __forceinline__ int rbuf_gather(const unsigned long long* cw, int n, Thresh th, unsigned long long* out,
-                                           int cap, uint32_t& cnt) {
-  if (threadIdx.x == 0) cnt = 0u;
-  __syncthreads();
-  for (int base = 0; base < n; base += kRT) {
-    const int i = base + static_cast<int>(threadIdx.x);
-    const unsigned long long w = i < n ? cw[i] : 0ull;
-    const bool keep = w != 0ull && kept_by(static_cast<uint32_t>(w >> 32),
-                                          static_cast<int32_t>(~static_cast<uint32_t>(w)), th.key, th.idx);
-    const uint32_t pos = rwarp_reserve(keep ? 1u : 0u, cnt);
-    if (keep && pos < static_cast<uint32_t>(cap)) out[pos] = w;
+                                           int cap, unsigned long long* red) {
+  constexpr int per = kRCap / kRT;
+  unsigned long long w[per];
+  uint32_t c = 0;
+#pragma unroll
+  for (int e = 0; e < per; ++e) {
+    const int i = per * static_cast<int>(threadIdx.x) + e;
+    w[e] = i < n ? cw[i] : 0ull;
+    const bool keep = w[e] != 0ull && kept_by(static_cast<uint32_t>(w[e] >> 32),
+                                              static_cast<int32_t>(~static_cast<uint32_t>(w[e])), th.key, th.idx);
+    w[e] = keep ? w[e] : 0ull;
+    c += keep ? 1u : 0u;
+  }
+  uint32_t tot;
+  uint32_t pos = block_excl_scan_u32(c, &tot, red);
+#pragma unroll
+  for (int e = 0; e < per; ++e) {
+    if (w[e] != 0ull) {
+      if (pos < static_cast<uint32_t>(cap)) out[pos] = w[e];
+      ++pos;
+    }
   }
   __syncthreads();
-  const int m = static_cast<int>(cnt) < cap ? static_cast<int>(cnt) : cap;
-  __syncthreads();
-  return m;
+  return static_cast<int>(tot) < cap ? static_cast<int>(tot) : cap;
 }
 
 // ---- the sample ----------------------------------------------------------------------------
@@ -1081,7 +1091,7 @@ __device__ __noinline__ int32_t rk_row(const RowCtx& rc, const RowSmem& sm, uint
     return idx;
   }
   const Thresh tk = n > keff ? rbuf_kth(sm.cw, kRCap, keff, mx, mn, sm.hist, sm.wbuf, sm.red, sm.misc) : kKeepAll;
-  const int ns = rbuf_gather(sm.cw, kRCap, tk, sm.wbuf, kTopKMax, s_cnt);  // the k survivors
+  const int ns = rbuf_gather(sm.cw, kRCap, tk, sm.wbuf, kTopKMax, sm.red);  // the k survivors
   Thresh th = kKeepAll;
   if (topp_on && ns > 1) th = rk_topp(sm.wbuf, ns, M, p, sm.hist, sm.cw, sm.red, sm.misc);
   unsigned long long rb = 0, first = 0;
