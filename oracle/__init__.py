@@ -65,8 +65,10 @@ def sample_arrays(logits: np.ndarray, dtype: str, top_k, top_p, temperature, q, 
     top_k = np.ascontiguousarray(top_k, dtype=np.int32)
     top_p = np.ascontiguousarray(top_p, dtype=np.float32)
     temperature = np.ascontiguousarray(temperature, dtype=np.float32)
-    q = np.ascontiguousarray(q, dtype=np.float32)
-    assert q.shape == (B, V) and top_k.shape == (B,) and top_p.shape == (B,) and temperature.shape == (B,)
+    if q is not None:  # None: sampling off (greedy)
+        q = np.ascontiguousarray(q, dtype=np.float32)
+        assert q.shape == (B, V)
+    assert top_k.shape == (B,) and top_p.shape == (B,) and temperature.shape == (B,)
     if seen_indptr is not None:
         seen_indptr = np.ascontiguousarray(seen_indptr, dtype=np.int32)
         seen_ids = np.ascontiguousarray(seen_ids, dtype=np.int32)

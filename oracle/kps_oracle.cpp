@@ -43,6 +43,8 @@
 //     argmax with the lower index winning an exact tie, NaN scores ignored,
 //     the pi-first element if every score is NaN;
 //   * filtered output: the transformed value at kept positions, -inf elsewhere.
+//   * sampling off (q absent): the first element of the order in the kept set,
+//     i.e. the argmax of the filtered row with the lowest index among equals.
 
 #include <algorithm>
 #include <cmath>
@@ -141,6 +143,18 @@ RowResult sample_row(std::vector<float>& x, int64_t V, int32_t k, float p, float
     topp_gap = std::min(std::fabs(lo), std::fabs(hi)) / target;
   }
 
+  // Sampling off (no q) [NPU scenario table: Sample disabled; MM10 generation loop and
+  // "greedy mode": without sampling the next token is the argmax of the filtered logits,
+  // the first one among equal maxima]: the first element of the order, which every
+  // kept set holds.
+  if (!qrow) {
+    if (out_row) {
+      for (int64_t v = 0; v < V; ++v) out_row[v] = NEG_INF;
+      for (int64_t i = 0; i < nP; ++i) out_row[order[i]] = x[order[i]];
+    }
+    return RowResult{order[0], nP, std::numeric_limits<double>::infinity(), topp_gap};
+  }
+
   // Exponential race [NPU Sample]: argmax of (e / S_P) / (q + eps).
   double SP = 0.0;
   for (int64_t i = 0; i < nP; ++i) SP += e[i];
@@ -177,6 +191,7 @@ extern "C" {
 
 // Returns 0 on success, 1 on an invalid argument.  dtype: 0 = fp32, 1 = bf16.
 // seen_indptr / seen_ids / penalty may all be NULL (no penalty).
+// q may be NULL: sampling off (the first element of the kept set's order).
 // out_filtered may be NULL when need_logits == 0.  The three diagnostic
 // outputs (kept count, race gap, top-p gap per row) may be NULL.
 int kpso_sample(const void* logits, int dtype, int64_t B, int64_t V,
@@ -185,7 +200,7 @@ int kpso_sample(const void* logits, int dtype, int64_t B, int64_t V,
                 const float* q, float eps, int need_logits,
                 int64_t* out_idx, float* out_filtered,
                 int64_t* out_kept, double* out_race_gap, double* out_topp_gap) {
-  if (B < 0 || V < 1 || !logits || !top_k || !top_p || !temperature || !q || !out_idx)
+  if (B < 0 || V < 1 || !logits || !top_k || !top_p || !temperature || !out_idx)
     return 1;
   if (dtype != 0 && dtype != 1) return 1;
   if (need_logits && !out_filtered) return 1;
@@ -207,7 +222,7 @@ int kpso_sample(const void* logits, int dtype, int64_t B, int64_t V,
       if (nids < 0) nids = 0;
     }
     RowResult r = sample_row(x, V, top_k[b], top_p[b], temperature[b], ids, nids, pen_on,
-                             pen_on ? penalty[b] : 1.0f, q + b * V, eps,
+                             pen_on ? penalty[b] : 1.0f, q ? q + b * V : nullptr, eps,
                              need_logits ? out_filtered + b * V : nullptr);
     out_idx[b] = r.idx;
     if (out_kept) out_kept[b] = r.kept;

@@ -373,3 +373,21 @@ def test_race_exact_tie_takes_lower_index():
     # mirror the vocabulary: the winner is again the lower index of the tied pair
     r = run1(x[::-1], top_k=0, top_p=1.0, q=q[::-1])
     assert r["idx"][0] == 1
+
+
+def test_sampling_off_takes_the_first_of_the_order():
+    """q absent (sampling off): the argmax of the filtered row, the lowest index among equal
+    maxima [NPU scenario table, Sample disabled; MM10 greedy mode]; the kept set and the
+    filtered row are those of a sampled call."""
+    inp = _rows(6)
+    x = _transformed(inp)
+    off = oracle.sample_arrays(inp.logits, "f32", inp.top_k, inp.top_p, inp.temperature, None)
+    on = oracle.sample_arrays(inp.logits, "f32", inp.top_k, inp.top_p, inp.temperature, inp.q)
+    for b in range(inp.B):
+        assert off["idx"][b] == _order_first(x[b])
+        assert off["kept"][b] == on["kept"][b]
+        assert np.array_equal(off["filtered"][b], on["filtered"][b])
+        assert math.isinf(off["race_gap"][b])
+    # equal maxima: the lower index
+    r = oracle.sample_arrays(np.array([[3.0, 5.0, 5.0, -1.0]], np.float32), "f32", [0], [0.99], [1.0], None)
+    assert r["idx"][0] == 1
