@@ -142,12 +142,14 @@ def query_launch(B: int, V: int, dtype: torch.dtype = torch.float32) -> dict:
 
 
 def sample(logits: torch.Tensor, top_k: torch.Tensor, top_p: torch.Tensor, temperature: torch.Tensor,
-           q: torch.Tensor, *, seen_indptr: Optional[torch.Tensor] = None, seen_ids: Optional[torch.Tensor] = None,
+           q: Optional[torch.Tensor], *, seen_indptr: Optional[torch.Tensor] = None, seen_ids: Optional[torch.Tensor] = None,
            penalty: Optional[torch.Tensor] = None, eps: float = 1e-20, need_logits: bool = False,
            out_idx: Optional[torch.Tensor] = None, out_filtered: Optional[torch.Tensor] = None,
            workspace: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None):
     """One fused sampling step on the GPU (asynchronous on `stream`).
 
+    q: the race's Exp(1) draws [B, V] fp32, or None to sample off (each row's index is
+    the first element of its kept set's order: the argmax of the filtered row).
     Returns (out_idx int64[B], out_filtered float32[B,V] or None).
     """
     lib = load_library()
@@ -162,7 +164,8 @@ def sample(logits: torch.Tensor, top_k: torch.Tensor, top_p: torch.Tensor, tempe
     _check(top_k, "top_k", torch.int32, (B,), dev)
     _check(top_p, "top_p", torch.float32, (B,), dev)
     _check(temperature, "temperature", torch.float32, (B,), dev)
-    _check(q, "q", torch.float32, (B, V), dev)
+    if q is not None:
+        _check(q, "q", torch.float32, (B, V), dev)
     if seen_indptr is not None:
         _check(seen_indptr, "seen_indptr", torch.int32, (B + 1,), dev)
         if seen_ids is None or penalty is None:

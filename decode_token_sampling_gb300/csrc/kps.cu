@@ -1414,10 +1414,10 @@ __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P)
     }
 
     // ---- exponential race over the kept set, and the filtered-logit write --------------
-    const float* qrow = P.q + row * V;
+    const float* qrow = P.q ? P.q + row * V : nullptr;  // none: sampling off
     unsigned long long rb = 0;
-    if (single) {
-      // nothing to race
+    if (single || (cand_mode && !qrow)) {
+      // nothing to race (sampling off takes the first element of the order below)
     } else if (cand_mode) {
       for (int i = threadIdx.x; i < ncand; i += kThreads) {
         const uint32_t key = c.cand_key[i];
@@ -1453,7 +1453,7 @@ __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P)
               if (4 * g + e < n) orow[4 * g + e] = kp[e] ? vv[e] : -INFINITY;
           }
         }
-        if (!nk) continue;
+        if (!nk || !qrow) continue;
         float qq[4];
         if (nk == 4 && vec) {
           const float4 q4 = __ldcs(reinterpret_cast<const float4*>(qrow + c0) + g);
@@ -1859,13 +1859,13 @@ kps_status kps_sample(const void* logits, kps_dtype dt, int64_t B, int64_t V, co
     return KPS_ERR_WORKSPACE;
   if (B == 0) return KPS_OK;
   if (B > INT32_MAX / 16) return KPS_ERR_INVALID_ARG;
-  if (!logits || !top_k || !top_p || !temperature || !q || !out_idx) return KPS_ERR_INVALID_ARG;
+  if (!logits || !top_k || !top_p || !temperature || !out_idx) return KPS_ERR_INVALID_ARG;  // q: may be NULL
   if (need_logits && !out_filtered) return KPS_ERR_INVALID_ARG;
   const bool pen = seen_indptr && seen_ids && penalty;
 
   const size_t esize = dt == KPS_BF16 ? 2 : 4;
   const bool aligned = (reinterpret_cast<uintptr_t>(logits) % 16 == 0) && ((V * esize) % 16 == 0) &&
-                       (reinterpret_cast<uintptr_t>(q) % 16 == 0) && (V % 4 == 0) &&
+                       (reinterpret_cast<uintptr_t>(q) % 16 == 0) && (V % 4 == 0) &&  // a NULL q is aligned
                        (!need_logits || reinterpret_cast<uintptr_t>(out_filtered) % 16 == 0);
   const bool want_row =
       aligned && (kps::g_policy >= 2 || (kps::g_policy == 0 && B >= kps::kRowMinRows));

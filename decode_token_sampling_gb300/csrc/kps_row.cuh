@@ -1005,10 +1005,12 @@ __device__ __forceinline__ void rlist_race(const unsigned long long* kl, int n, 
     if (w == 0ull || !kept_by(key, idx, th.key, th.idx)) continue;
     first = w > first ? w : first;
     const float y = kfloat(key);
-    const float r = __fdiv_rn(softmax_weight(y, M), __fadd_rn(__ldg(rc.q + idx), eps));
-    if (!isnan(r)) {
-      const unsigned long long c = order_word(fkey(r), idx);
-      rb = c > rb ? c : rb;
+    if (rc.q) {
+      const float r = __fdiv_rn(softmax_weight(y, M), __fadd_rn(__ldg(rc.q + idx), eps));
+      if (!isnan(r)) {
+        const unsigned long long c = order_word(fkey(r), idx);
+        rb = c > rb ? c : rb;
+      }
     }
     if (rc.out) rc.out[idx] = y;
   }
@@ -1205,11 +1207,13 @@ __device__ __noinline__ void rrow_race_write(const RowCtx& rc, Thresh th, float 
     unpack16<kBF16>(ld_row16(rc.x + g, pol), v);
     const uint32_t bits = rseen_bits<G>(rc.bitmap, rc.pen_on, g);
     float qv[G];
-    const float4* q4 = reinterpret_cast<const float4*>(rc.q) + g * (G / 4);
+    if (rc.q) {
+      const float4* q4 = reinterpret_cast<const float4*>(rc.q) + g * (G / 4);
 #pragma unroll
-    for (int h = 0; h < G / 4; ++h) {
-      const float4 t = __ldcs(q4 + h);
-      qv[4 * h] = t.x; qv[4 * h + 1] = t.y; qv[4 * h + 2] = t.z; qv[4 * h + 3] = t.w;
+      for (int h = 0; h < G / 4; ++h) {
+        const float4 t = __ldcs(q4 + h);
+        qv[4 * h] = t.x; qv[4 * h + 1] = t.y; qv[4 * h + 2] = t.z; qv[4 * h + 3] = t.w;
+      }
     }
     float o[G];
 #pragma unroll
@@ -1222,10 +1226,12 @@ __device__ __noinline__ void rrow_race_write(const RowCtx& rc, Thresh th, float 
       if (kept) {
         const unsigned long long ow = order_word(key, idx);
         first = ow > first ? ow : first;
-        const float r = __fdiv_rn(softmax_weight(y, M), __fadd_rn(qv[e], eps));
-        if (!isnan(r)) {
-          const unsigned long long c = order_word(fkey(r), idx);
-          rb = c > rb ? c : rb;
+        if (rc.q) {
+          const float r = __fdiv_rn(softmax_weight(y, M), __fadd_rn(qv[e], eps));
+          if (!isnan(r)) {
+            const unsigned long long c = order_word(fkey(r), idx);
+            rb = c > rb ? c : rb;
+          }
         }
       }
     }
@@ -1361,6 +1367,7 @@ __device__ __noinline__ unsigned long long rp_pass_a(const RowCtx& rc, float H, 
   const unsigned long long pol = l2_policy_last();
   const uint4* xr = rc.x;
   const float4* qr = reinterpret_cast<const float4*>(rc.q);
+  const bool race = rc.q != nullptr;  // sampling off: no race words
   const int g0 = rc.g0, g1 = rc.g1;
   const uint32_t* bitmap = rc.bitmap;
   const bool pen_on = rc.pen_on, identity = rc.identity;
@@ -1379,7 +1386,7 @@ __device__ __noinline__ unsigned long long rp_pass_a(const RowCtx& rc, float H, 
       w[u] = g < g1 ? ld_row16(xr + g, pol) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
       for (int hh = 0; hh < G / 4; ++hh)
-        qv[u][hh] = g < g1 ? __ldcs(qr + g * (G / 4) + hh) : make_float4(0.f, 0.f, 0.f, 0.f);
+        qv[u][hh] = (race && g < g1) ? __ldcs(qr + g * (G / 4) + hh) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int u = 0; u < kUA; ++u) {
@@ -1405,8 +1412,10 @@ __device__ __noinline__ unsigned long long rp_pass_a(const RowCtx& rc, float H, 
           sh_red_add(&h[kRPBins + pw.b], pw.w24 >> 12);
           const float4 q4 = qv[u][e / 4];
           const float qe = (e & 3) == 0 ? q4.x : (e & 3) == 1 ? q4.y : (e & 3) == 2 ? q4.z : q4.w;
-          const uint32_t key = prace_key(pw.wf, qe, eps);
-          sh_max_word(smem_u32(ub + pw.b), key, order_word(key, g * G + e));
+          if (race) {
+            const uint32_t key = prace_key(pw.wf, qe, eps);
+            sh_max_word(smem_u32(ub + pw.b), key, order_word(key, g * G + e));
+          }
         }
       }
     }
@@ -1945,7 +1954,7 @@ __device__ __noinline__ int32_t rwide_row(const RowCtx& rc, const RowSmem& sm, c
       const int32_t idx = static_cast<int32_t>(~static_cast<uint32_t>(wd));
       if (!kept_by(key, idx, bth.key, bth.idx)) continue;
       const float y = kfloat(key);
-      const uint32_t rk = prace_key(pweight(y, H).wf, __ldg(rc.q + idx), eps);
+      const uint32_t rk = rc.q ? prace_key(pweight(y, H).wf, __ldg(rc.q + idx), eps) : 0u;
       const float r = rk ? prace_value(rk, f24b) : -1.0f;
       if (rk && (r > rbest || (r == rbest && idx < ridx))) {
         rbest = r;
@@ -2096,7 +2105,7 @@ __device__ __forceinline__ RowFlags row_setup(const Params& P, int64_t row, cons
   f.topp_on = !f.single && !p_nan && f.p > 0.0f && f.p < 1.0f;
   RowCtx& rc = *rcp;
   rc.x = reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(P.logits) + row * P.V * esize);
-  rc.q = P.q + row * P.V;
+  rc.q = P.q ? P.q + row * P.V : nullptr;  // none: sampling off
   rc.out = P.need_logits ? P.out_filtered + row * P.V : nullptr;
   rc.V = V;
   rc.nv = V / G;

@@ -98,7 +98,13 @@ int64_t kps_max_vocab(kps_dtype dt);
  *                 runs only when all three of seen_indptr, seen_ids and
  *                 penalty are non-NULL.
  *   q             [B, V] fp32 race weights (Exp(1) draws supplied by the
- *                 caller).  Required.
+ *                 caller), or NULL to sample off: each row's index is then
+ *                 the first element of its kept set's order (the argmax of
+ *                 the filtered row, the lowest index among equal maxima;
+ *                 the Ascend page's scenario table lets the Sample stage be
+ *                 disabled, and the MiniMind inference chapter's greedy mode
+ *                 takes that argmax).  The filtered row is the same either
+ *                 way.
  *   eps           added to q before dividing; must be >= 0 and finite.
  *   need_logits   non-zero: write out_filtered.
  *   out_idx       [B] int64 chosen token per row.

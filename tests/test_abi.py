@@ -69,7 +69,7 @@ def test_host_validation_without_gpu(lib):
     assert _call(lib, workspace_bytes=8) == 3
     assert _call(lib, B=0) == 0  # valid no-op, nothing launched
     assert _call(lib, logits=None) == 1
-    assert _call(lib, q=None) == 1
+    assert _call(lib, q=None) not in (1, 3)  # sampling off: a valid call (here it fails only for want of a GPU)
     assert _call(lib, out_idx=None) == 1
     assert _call(lib, need_logits=1, out_filtered=None) == 1
 

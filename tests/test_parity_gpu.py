@@ -242,3 +242,24 @@ def test_pre_pass_records_on_odd_rows(case):
         assert int(ws[256:].count_nonzero().item()) == 0
     finally:
         kps.set_kernel_policy(kps.KERNEL_AUTO)
+
+
+@pytest.mark.parametrize("name", ["small_mixed", "batch256_penalty", "flat_nucleus", "single_row_long"])
+def test_sampling_off(name, kernel):
+    """q absent: every row's index is the first element of its kept set's order (the
+    oracle's reading of sampling off); the filtered row is unchanged."""
+    inp = make_workload(name)
+    inp.q = None
+    inp.need_logits = True
+    ref = oracle.sample(inp)
+    gi, gf = run_gpu(inp)
+    compare(inp, ref, gi, gf, f"{name} [sampling off]")
+
+
+def test_sampling_off_edge_rows():
+    """Sampling off on rows with NaN/-inf logits, ties, penalties and edge parameters."""
+    inp = make_random(24, 5003, seed=91, ties=True, special=True, penalty=1.5, n_seen=50)
+    inp.q = None
+    ref = oracle.sample(inp)
+    gi, gf = run_gpu(inp)
+    compare(inp, ref, gi, gf, "edge rows [sampling off]")
