@@ -43,6 +43,10 @@ def _load() -> ctypes.CDLL:
         lib.kpso_sample.restype = ctypes.c_int
         lib.kpso_sample.argtypes = [P, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, P, P, P, P, P, P,
                                     P, ctypes.c_float, ctypes.c_int, P, P, P, P, P]
+        lib.kpso_exp_draws.restype = ctypes.c_int
+        lib.kpso_exp_draws.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_uint64, ctypes.c_uint64, P]
+        lib.kpso_philox4x32_10.restype = None
+        lib.kpso_philox4x32_10.argtypes = [P, ctypes.c_uint32, ctypes.c_uint32]
         _lib = lib
     return _lib
 
@@ -92,3 +96,19 @@ def sample(inp, need_logits: Optional[bool] = None) -> dict:
     nl = inp.need_logits if need_logits is None else need_logits
     return sample_arrays(inp.logits, inp.dtype, inp.top_k, inp.top_p, inp.temperature, inp.q, inp.eps,
                          nl, inp.seen_indptr, inp.seen_ids, inp.penalty)
+
+
+def exp_draws(B: int, V: int, seed: int, step: int = 0) -> np.ndarray:
+    """The generated Exp(1) draws q[B, V] of a seeded call (Philox4x32-10, see kps_oracle.cpp)."""
+    q = np.empty((B, V), dtype=np.float32)
+    if _load().kpso_exp_draws(B, V, seed & (2**64 - 1), step & (2**64 - 1), _ptr(q)) != 0:
+        raise ValueError("bad sizes")
+    return q
+
+
+def philox4x32_10(counter, key) -> list:
+    """One Philox4x32-10 block: four 32-bit counter words and two key words in, four words out."""
+    c = np.array(counter, dtype=np.uint32)
+    _load().kpso_philox4x32_10(c.ctypes.data_as(ctypes.c_void_p), int(key[0]), int(key[1]))
+    return [int(x) for x in c]
+

@@ -232,4 +232,46 @@ int kpso_sample(const void* logits, int dtype, int64_t B, int64_t V,
   return 0;
 }
 
+// ---- Exp(1) draws from a counter-based generator (sampling without a supplied q) ---------
+//
+// Philox4x32-10 [Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3",
+// SC'11, section 4 (the Philox S-box: a 32x32 -> 64-bit multiply whose halves are mixed
+// into the other words, 10 rounds, the key bumped by the Weyl increments between rounds)
+// and its table of round constants for Philox-4x32].
+static void philox4x32_10(uint32_t c[4], uint32_t k0, uint32_t k1) {
+  for (int round = 0; round < 10; ++round) {
+    const uint64_t p0 = static_cast<uint64_t>(0xD2511F53u) * c[0];
+    const uint64_t p1 = static_cast<uint64_t>(0xCD9E8D57u) * c[2];
+    const uint32_t hi0 = static_cast<uint32_t>(p0 >> 32), lo0 = static_cast<uint32_t>(p0);
+    const uint32_t hi1 = static_cast<uint32_t>(p1 >> 32), lo1 = static_cast<uint32_t>(p1);
+    const uint32_t n0 = hi1 ^ c[1] ^ k0, n1 = lo1, n2 = hi0 ^ c[3] ^ k1, n3 = lo0;
+    c[0] = n0; c[1] = n1; c[2] = n2; c[3] = n3;
+    k0 += 0x9E3779B9u;  // the Weyl increments of the key
+    k1 += 0xBB67AE85u;
+  }
+}
+
+// The draw of row b, token v at decode step `step` under `seed`: Philox4x32-10 with key
+// (seed low, seed high) on the counter (v / 4, b, step low, step high), word v mod 4;
+// u = (2 * (word >> 9) + 1) * 2^-24 in (0, 1) (exact in fp32); q = -log(u) rounded to fp32.
+static float exp_draw(uint64_t seed, uint64_t step, int64_t b, int64_t v) {
+  uint32_t c[4] = {static_cast<uint32_t>(v >> 2), static_cast<uint32_t>(b), static_cast<uint32_t>(step),
+                   static_cast<uint32_t>(step >> 32)};
+  philox4x32_10(c, static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
+  const uint32_t w = c[v & 3];
+  const double u = static_cast<double>(2u * (w >> 9) + 1u) * (1.0 / 16777216.0);
+  return static_cast<float>(-std::log(u));
+}
+
+// The raw generator, for its known-answer tests: c (4 words) is replaced by its output.
+void kpso_philox4x32_10(uint32_t* c, uint32_t k0, uint32_t k1) { philox4x32_10(c, k0, k1); }
+
+// q[B, V] of the generated Exp(1) draws (the q a seeded kps call races with).
+int kpso_exp_draws(int64_t B, int64_t V, uint64_t seed, uint64_t step, float* q) {
+  if (B < 0 || V < 1 || !q) return 1;
+  for (int64_t b = 0; b < B; ++b)
+    for (int64_t v = 0; v < V; ++v) q[b * V + v] = exp_draw(seed, step, b, v);
+  return 0;
+}
+
 }  // extern "C"

@@ -391,3 +391,49 @@ def test_sampling_off_takes_the_first_of_the_order():
     # equal maxima: the lower index
     r = oracle.sample_arrays(np.array([[3.0, 5.0, 5.0, -1.0]], np.float32), "f32", [0], [0.99], [1.0], None)
     assert r["idx"][0] == 1
+
+
+# ----------------------------------------------------------------------------------------------
+# Generated Exp(1) draws (a seeded call races with these instead of a supplied q)
+# ----------------------------------------------------------------------------------------------
+
+def test_philox_known_answers():
+    """The generator reproduces the published Philox4x32-10 known-answer vectors."""
+    pairs = read_pairs("philox4x32_10_kat.txt")
+    hexes = lambda s: [int(t, 16) for t in s.split()]
+    n = 0
+    for i in range(0, len(pairs), 3):
+        (kc, c), (kk, k), (ko, o) = pairs[i:i + 3]
+        assert (kc, kk, ko) == ("counter", "key", "out")
+        assert oracle.philox4x32_10(hexes(c), hexes(k)) == hexes(o)
+        n += 1
+    assert n == 3
+
+
+def test_exp_draws_follow_their_definition():
+    """Each draw is -log(u) of its own Philox word: counter (v/4, row, step), word v mod 4."""
+    seed, step = 0x0123456789ABCDEF, 7
+    q = oracle.exp_draws(3, 10, seed, step)
+    for b in range(3):
+        for v in range(10):
+            w = oracle.philox4x32_10([v // 4, b, step & 0xFFFFFFFF, step >> 32],
+                                     [seed & 0xFFFFFFFF, seed >> 32])[v % 4]
+            u = (2 * (w >> 9) + 1) / 2.0**24
+            assert q[b, v] == np.float32(-math.log(u))
+    # a different step or seed gives different draws
+    assert not np.array_equal(q, oracle.exp_draws(3, 10, seed, step + 1))
+    assert not np.array_equal(q, oracle.exp_draws(3, 10, seed + 1, step))
+
+
+def test_exp_draws_are_exp1():
+    """Kolmogorov-Smirnov distance to the Exp(1) distribution, mean and variance, and no
+    correlation between neighbouring tokens or rows, over 10^6 draws."""
+    q = oracle.exp_draws(100, 10000, seed=2024, step=3).astype(np.float64)
+    x = np.sort(q.ravel())
+    n = x.size
+    cdf = 1.0 - np.exp(-x)
+    ks = max(np.max(np.arange(1, n + 1) / n - cdf), np.max(cdf - np.arange(0, n) / n))
+    assert ks < 1.95 / math.sqrt(n)  # about the 0.1% critical value
+    assert abs(x.mean() - 1.0) < 5e-3 and abs(x.var() - 1.0) < 1e-2
+    assert abs(np.corrcoef(q[:, :-1].ravel(), q[:, 1:].ravel())[0, 1]) < 5e-3
+    assert abs(np.corrcoef(q[:-1].ravel(), q[1:].ravel())[0, 1]) < 5e-3
