@@ -51,6 +51,9 @@ def load_library() -> ctypes.CDLL:
     lib.kps_last_device_status.argtypes = [P, P, ctypes.POINTER(I32)]
     lib.kps_status_string.restype = ctypes.c_char_p
     lib.kps_status_string.argtypes = [I32]
+    lib.kps_sample_seeded.restype = I32
+    lib.kps_sample_seeded.argtypes = [P, I32, I64, I64, P, P, P, P, P, P, ctypes.c_uint64, ctypes.c_uint64,
+                                      ctypes.c_float, I32, P, P, P, ctypes.c_size_t, P]
     lib.kps_set_kernel_policy.restype = I32
     lib.kps_set_kernel_policy.argtypes = [I32]
     lib.kps_get_kernel_policy.restype = I32
@@ -145,11 +148,14 @@ def sample(logits: torch.Tensor, top_k: torch.Tensor, top_p: torch.Tensor, tempe
            q: Optional[torch.Tensor], *, seen_indptr: Optional[torch.Tensor] = None, seen_ids: Optional[torch.Tensor] = None,
            penalty: Optional[torch.Tensor] = None, eps: float = 1e-20, need_logits: bool = False,
            out_idx: Optional[torch.Tensor] = None, out_filtered: Optional[torch.Tensor] = None,
-           workspace: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None):
+           workspace: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None,
+           seed: Optional[int] = None, step: int = 0):
     """One fused sampling step on the GPU (asynchronous on `stream`).
 
     q: the race's Exp(1) draws [B, V] fp32, or None to sample off (each row's index is
     the first element of its kept set's order: the argmax of the filtered row).
+    seed: race with draws generated from (seed, step) instead (q must then be None;
+    kps_sample_seeded in include/kps.h defines them).
     Returns (out_idx int64[B], out_filtered float32[B,V] or None).
     """
     lib = load_library()
@@ -165,6 +171,8 @@ def sample(logits: torch.Tensor, top_k: torch.Tensor, top_p: torch.Tensor, tempe
     _check(top_p, "top_p", torch.float32, (B,), dev)
     _check(temperature, "temperature", torch.float32, (B,), dev)
     if q is not None:
+        if seed is not None:
+            raise ValueError("pass q or seed, not both")
         _check(q, "q", torch.float32, (B, V), dev)
     if seen_indptr is not None:
         _check(seen_indptr, "seen_indptr", torch.int32, (B + 1,), dev)
@@ -184,12 +192,19 @@ def sample(logits: torch.Tensor, top_k: torch.Tensor, top_p: torch.Tensor, tempe
     if workspace is None:
         workspace = new_workspace(B, V, logits.dtype, dev)
     s = stream if stream is not None else torch.cuda.current_stream(dev)
-    st = lib.kps_sample(_ptr(logits), dt, B, V, _ptr(top_k), _ptr(top_p), _ptr(temperature), _ptr(seen_indptr),
-                        _ptr(seen_ids), _ptr(penalty), _ptr(q), float(eps), 1 if need_logits else 0,
-                        _ptr(out_idx), _ptr(out_filtered), _ptr(workspace), workspace.numel(),
-                        ctypes.c_void_p(s.cuda_stream))
+    if seed is not None:
+        st = lib.kps_sample_seeded(_ptr(logits), dt, B, V, _ptr(top_k), _ptr(top_p), _ptr(temperature),
+                                   _ptr(seen_indptr), _ptr(seen_ids), _ptr(penalty), int(seed) & (2**64 - 1),
+                                   int(step) & (2**64 - 1), float(eps), 1 if need_logits else 0, _ptr(out_idx),
+                                   _ptr(out_filtered), _ptr(workspace), workspace.numel(),
+                                   ctypes.c_void_p(s.cuda_stream))
+    else:
+        st = lib.kps_sample(_ptr(logits), dt, B, V, _ptr(top_k), _ptr(top_p), _ptr(temperature),
+                            _ptr(seen_indptr), _ptr(seen_ids), _ptr(penalty), _ptr(q), float(eps),
+                            1 if need_logits else 0, _ptr(out_idx), _ptr(out_filtered), _ptr(workspace),
+                            workspace.numel(), ctypes.c_void_p(s.cuda_stream))
     if st != 0:
-        raise KpsError(st, "kps_sample")
+        raise KpsError(st, "kps_sample_seeded" if seed is not None else "kps_sample")
     return out_idx, out_filtered
 
 

@@ -118,6 +118,8 @@ struct Params {
   int exact;    // row kernel: skip the sample and the band, always select over the whole row
   unsigned char* pre;  // row kernel: per-row records of the pre-pass (nullptr: no pre-pass)
   int pre_rows;        // records available (the first pre_rows top-p-only rows use them)
+  int gen;             // race with generated Exp(1) draws (q is then nullptr)
+  unsigned long long seed, step;  // their generator's key and the decode step
 };
 
 constexpr int kMaxRowList = 256;  // rows one worker (CTA or cluster) may own in a filtered launch
@@ -223,6 +225,44 @@ __device__ __forceinline__ unsigned long long order_word(uint32_t key, int32_t i
 // as hi + lo (Knuth's TwoSum) and the exponential is corrected to first order,
 // e * (1 + lo), so the weight does not inherit the rounding of the subtraction.
 // x == M gives exactly 1 (which keeps +-inf maxima finite).
+// ---- generated Exp(1) draws ------------------------------------------------------------
+//
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as 1, 2,
+// 3", SC'11, section 4 and its Philox-4x32 round constants): ten rounds of two
+// 32x32 -> 64-bit products whose halves are mixed into the other counter words, the key
+// bumped by its Weyl increments between rounds.  The draw of row b, token v at step s
+// under seed k: counter (v / 4, b, s low, s high), key (k low, k high), word v mod 4,
+// u = (2 (w >> 9) + 1) 2^-24, q = -log(u).
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int round = 0; round < 10; ++round) {
+    const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+    const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return c;
+}
+__device__ __forceinline__ float exp_of_word(uint32_t w) {
+  return -logf(__fmul_rn(static_cast<float>(2u * (w >> 9) + 1u), 5.9604644775390625e-8f));
+}
+// The four draws of tokens 4g .. 4g + 3 of a row.
+__device__ __forceinline__ float4 gen_q4(unsigned long long seed, unsigned long long step, int64_t row, int64_t g) {
+  const uint4 w = philox4x32_10(make_uint4(static_cast<uint32_t>(g), static_cast<uint32_t>(row),
+                                           static_cast<uint32_t>(step), static_cast<uint32_t>(step >> 32)),
+                                static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
+  return make_float4(exp_of_word(w.x), exp_of_word(w.y), exp_of_word(w.z), exp_of_word(w.w));
+}
+// The draw of token v of a row.
+__device__ __forceinline__ float gen_q1(unsigned long long seed, unsigned long long step, int64_t row, int64_t v) {
+  const uint4 w = philox4x32_10(make_uint4(static_cast<uint32_t>(v >> 2), static_cast<uint32_t>(row),
+                                           static_cast<uint32_t>(step), static_cast<uint32_t>(step >> 32)),
+                                static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
+  const int e = static_cast<int>(v & 3);
+  return exp_of_word(e == 0 ? w.x : e == 1 ? w.y : e == 2 ? w.z : w.w);
+}
+
 __device__ __forceinline__ float softmax_weight(float x, float M) {
   if (x == M) return 1.0f;
   float s = __fsub_rn(x, M);
@@ -1414,9 +1454,10 @@ __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P)
     }
 
     // ---- exponential race over the kept set, and the filtered-logit write --------------
-    const float* qrow = P.q ? P.q + row * V : nullptr;  // none: sampling off
+    const float* qrow = P.q ? P.q + row * V : nullptr;  // none: sampling off or generated draws
+    const bool race = qrow != nullptr || P.gen != 0;
     unsigned long long rb = 0;
-    if (single || (cand_mode && !qrow)) {
+    if (single || (cand_mode && !race)) {
       // nothing to race (sampling off takes the first element of the order below)
     } else if (cand_mode) {
       for (int i = threadIdx.x; i < ncand; i += kThreads) {
@@ -1424,7 +1465,8 @@ __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P)
         const int32_t idx = c.cand_idx[i];
         if (!kept_by(key, idx, th.key, th.idx)) continue;
         const float w = softmax_weight(kfloat(key), M);
-        const float r = __fdiv_rn(w, __fadd_rn(__ldg(qrow + idx), P.eps));
+        const float qv = P.gen ? gen_q1(P.seed, P.step, row, idx) : __ldg(qrow + idx);
+        const float r = __fdiv_rn(w, __fadd_rn(qv, P.eps));
         if (isnan(r)) continue;
         const unsigned long long cand = order_word(fkey(r), idx);
         rb = cand > rb ? cand : rb;
@@ -1453,9 +1495,13 @@ __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P)
               if (4 * g + e < n) orow[4 * g + e] = kp[e] ? vv[e] : -INFINITY;
           }
         }
-        if (!nk || !qrow) continue;
+        if (!nk || !race) continue;
         float qq[4];
-        if (nk == 4 && vec) {
+        if (P.gen) {
+          // c0 is a multiple of 4: the group's four draws in one generator block
+          const float4 q4 = gen_q4(P.seed, P.step, row, (c0 >> 2) + g);
+          qq[0] = q4.x; qq[1] = q4.y; qq[2] = q4.z; qq[3] = q4.w;
+        } else if (nk == 4 && vec) {
           const float4 q4 = __ldcs(reinterpret_cast<const float4*>(qrow + c0) + g);
           qq[0] = q4.x; qq[1] = q4.y; qq[2] = q4.z; qq[3] = q4.w;
         } else {
@@ -1847,11 +1893,13 @@ kps_status kps_query_launch(int64_t B, int64_t V, kps_dtype dt, int* cluster_siz
   return KPS_OK;
 }
 
-kps_status kps_sample(const void* logits, kps_dtype dt, int64_t B, int64_t V, const int32_t* top_k,
-                      const float* top_p, const float* temperature, const int32_t* seen_indptr,
-                      const int32_t* seen_ids, const float* penalty, const float* q, float eps, int need_logits,
-                      int64_t* out_idx, float* out_filtered, void* workspace, size_t workspace_bytes,
-                      cudaStream_t stream) {
+// The sampling step; q given (or NULL) or, with gen, generated from (seed, step).
+static kps_status sample_impl(const void* logits, kps_dtype dt, int64_t B, int64_t V, const int32_t* top_k,
+                              const float* top_p, const float* temperature, const int32_t* seen_indptr,
+                              const int32_t* seen_ids, const float* penalty, const float* q, float eps,
+                              int need_logits, int64_t* out_idx, float* out_filtered, void* workspace,
+                              size_t workspace_bytes, cudaStream_t stream, int gen, unsigned long long seed,
+                              unsigned long long step) {
   if (dt != KPS_F32 && dt != KPS_BF16) return KPS_ERR_INVALID_ARG;
   if (V < 1 || V > INT32_MAX || B < 0) return KPS_ERR_INVALID_ARG;
   if (!(eps >= 0.0f) || std::isinf(eps)) return KPS_ERR_INVALID_ARG;
@@ -1892,7 +1940,10 @@ kps_status kps_sample(const void* logits, kps_dtype dt, int64_t B, int64_t V, co
   P.seen_indptr = pen ? seen_indptr : nullptr;
   P.seen_ids = pen ? seen_ids : nullptr;
   P.penalty = pen ? penalty : nullptr;
-  P.q = q;
+  P.q = gen ? nullptr : q;
+  P.gen = gen ? 1 : 0;
+  P.seed = seed;
+  P.step = step;
   P.eps = eps;
   P.need_logits = need_logits ? 1 : 0;
   P.out_idx = out_idx;
@@ -1978,6 +2029,24 @@ kps_status kps_sample(const void* logits, kps_dtype dt, int64_t B, int64_t V, co
   kps::t_last_kernel = 1;
   kps::t_last_launches = 1;
   return KPS_OK;
+}
+
+kps_status kps_sample(const void* logits, kps_dtype dt, int64_t B, int64_t V, const int32_t* top_k,
+                      const float* top_p, const float* temperature, const int32_t* seen_indptr,
+                      const int32_t* seen_ids, const float* penalty, const float* q, float eps, int need_logits,
+                      int64_t* out_idx, float* out_filtered, void* workspace, size_t workspace_bytes,
+                      cudaStream_t stream) {
+  return sample_impl(logits, dt, B, V, top_k, top_p, temperature, seen_indptr, seen_ids, penalty, q, eps,
+                     need_logits, out_idx, out_filtered, workspace, workspace_bytes, stream, 0, 0ull, 0ull);
+}
+
+kps_status kps_sample_seeded(const void* logits, kps_dtype dt, int64_t B, int64_t V, const int32_t* top_k,
+                             const float* top_p, const float* temperature, const int32_t* seen_indptr,
+                             const int32_t* seen_ids, const float* penalty, unsigned long long seed,
+                             unsigned long long step, float eps, int need_logits, int64_t* out_idx,
+                             float* out_filtered, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return sample_impl(logits, dt, B, V, top_k, top_p, temperature, seen_indptr, seen_ids, penalty, nullptr, eps,
+                     need_logits, out_idx, out_filtered, workspace, workspace_bytes, stream, 1, seed, step);
 }
 
 kps_status kps_set_kernel_policy(int policy) {

@@ -174,7 +174,7 @@ __device__ __forceinline__ float raw_floor(float tv, float T, bool identity) {
 
 struct RowCtx {
   const uint4* x;          // the row of logits as 16-byte vectors
-  const float* q;          // the row of q
+  const float* q;          // the row of q (nullptr: generated draws, or sampling off)
   float* out;              // the row of the filtered logits, or nullptr
   int V;
   int nv;                  // vectors in the row
@@ -185,7 +185,26 @@ struct RowCtx {
   float T;
   FixedDivisor div;        // T with its reciprocal
   bool identity;
+  bool race;               // a race is run: q given or generated (else sampling off)
+  bool gen;                // generated draws
+  unsigned long long seed, step;
+  int64_t row;             // the row (the generator's counter)
 };
+
+// The race's q of token idx, and of the four tokens 4h .. 4h + 3 (loaded, or generated).
+// (The generator is called out of line here, so the loaded-q code stays small.)
+__device__ __noinline__ float gen_q1_call(unsigned long long seed, unsigned long long step, int64_t row, int idx) {
+  return gen_q1(seed, step, row, idx);
+}
+__device__ __noinline__ float4 gen_q4_call(unsigned long long seed, unsigned long long step, int64_t row, int h) {
+  return gen_q4(seed, step, row, h);
+}
+__device__ __forceinline__ float rq1(const RowCtx& rc, int idx) {
+  return rc.gen ? gen_q1_call(rc.seed, rc.step, rc.row, idx) : __ldg(rc.q + idx);
+}
+__device__ __forceinline__ float4 rq4(const RowCtx& rc, int h) {
+  return rc.gen ? gen_q4_call(rc.seed, rc.step, rc.row, h) : __ldcs(reinterpret_cast<const float4*>(rc.q) + h);
+}
 
 // Seen-bits of the G elements of vector g (G divides 32, so they share one word).
 template <int G>
@@ -1005,8 +1024,8 @@ __device__ __forceinline__ void rlist_race(const unsigned long long* kl, int n, 
     if (w == 0ull || !kept_by(key, idx, th.key, th.idx)) continue;
     first = w > first ? w : first;
     const float y = kfloat(key);
-    if (rc.q) {
-      const float r = __fdiv_rn(softmax_weight(y, M), __fadd_rn(__ldg(rc.q + idx), eps));
+    if (rc.race) {
+      const float r = __fdiv_rn(softmax_weight(y, M), __fadd_rn(rq1(rc, idx), eps));
       if (!isnan(r)) {
         const unsigned long long c = order_word(fkey(r), idx);
         rb = c > rb ? c : rb;
@@ -1207,11 +1226,10 @@ __device__ __noinline__ void rrow_race_write(const RowCtx& rc, Thresh th, float 
     unpack16<kBF16>(ld_row16(rc.x + g, pol), v);
     const uint32_t bits = rseen_bits<G>(rc.bitmap, rc.pen_on, g);
     float qv[G];
-    if (rc.q) {
-      const float4* q4 = reinterpret_cast<const float4*>(rc.q) + g * (G / 4);
+    if (rc.race) {
 #pragma unroll
       for (int h = 0; h < G / 4; ++h) {
-        const float4 t = __ldcs(q4 + h);
+        const float4 t = rq4(rc, g * (G / 4) + h);
         qv[4 * h] = t.x; qv[4 * h + 1] = t.y; qv[4 * h + 2] = t.z; qv[4 * h + 3] = t.w;
       }
     }
@@ -1226,7 +1244,7 @@ __device__ __noinline__ void rrow_race_write(const RowCtx& rc, Thresh th, float 
       if (kept) {
         const unsigned long long ow = order_word(key, idx);
         first = ow > first ? ow : first;
-        if (rc.q) {
+        if (rc.race) {
           const float r = __fdiv_rn(softmax_weight(y, M), __fadd_rn(qv[e], eps));
           if (!isnan(r)) {
             const unsigned long long c = order_word(fkey(r), idx);
@@ -1359,15 +1377,17 @@ __device__ __forceinline__ void sh_max_word(uint32_t a, uint32_t key, unsigned l
 // (h[b], h[kRPBins + b]: a bin takes any row of at most 2^18 elements without overflow),
 // and per bin the best race word (race key, index; the lower index on equal keys) in
 // ub[b].  Returns the part's largest value as a key.
-template <bool kBF16>
-__device__ __noinline__ unsigned long long rp_pass_a(const RowCtx& rc, float H, float eps, uint32_t* h,
-                                                     unsigned long long* ub, unsigned long long* red) {
+template <bool kBF16, bool kGen>
+__device__ __noinline__ unsigned long long rp_pass_a_t(const RowCtx& rc, float H, float eps, uint32_t* h,
+                                                       unsigned long long* ub, unsigned long long* red) {
   constexpr int G = kBF16 ? 8 : 4;
   constexpr int kUA = kBF16 ? 1 : 2;  // vectors in flight per thread (q rides along)
   const unsigned long long pol = l2_policy_last();
   const uint4* xr = rc.x;
+  const bool race = rc.race;  // sampling off: no race words
   const float4* qr = reinterpret_cast<const float4*>(rc.q);
-  const bool race = rc.q != nullptr;  // sampling off: no race words
+  const unsigned long long seed = rc.seed, step = rc.step;
+  const int64_t row = rc.row;
   const int g0 = rc.g0, g1 = rc.g1;
   const uint32_t* bitmap = rc.bitmap;
   const bool pen_on = rc.pen_on, identity = rc.identity;
@@ -1386,7 +1406,9 @@ __device__ __noinline__ unsigned long long rp_pass_a(const RowCtx& rc, float H, 
       w[u] = g < g1 ? ld_row16(xr + g, pol) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
       for (int hh = 0; hh < G / 4; ++hh)
-        qv[u][hh] = (race && g < g1) ? __ldcs(qr + g * (G / 4) + hh) : make_float4(0.f, 0.f, 0.f, 0.f);
+        qv[u][hh] = (race && g < g1)
+                        ? (kGen ? gen_q4(seed, step, row, g * (G / 4) + hh) : __ldcs(qr + g * (G / 4) + hh))
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int u = 0; u < kUA; ++u) {
@@ -1423,6 +1445,13 @@ __device__ __noinline__ unsigned long long rp_pass_a(const RowCtx& rc, float H, 
   unsigned long long kmax = fkey(__fadd_rn(ymax, 0.0f)), dummy = 0;
   rblock_max2(kmax, dummy, red);
   return kmax;
+}
+
+// Pass A with q loaded or generated (one instantiation each, so neither pays for the other).
+template <bool kBF16>
+__device__ __forceinline__ unsigned long long rp_pass_a(const RowCtx& rc, float H, float eps, uint32_t* h,
+                                                        unsigned long long* ub, unsigned long long* red) {
+  return rc.gen ? rp_pass_a_t<kBF16, true>(rc, H, eps, h, ub, red) : rp_pass_a_t<kBF16, false>(rc, H, eps, h, ub, red);
 }
 
 // Pass B of top-p-only rows over this CTA's part, once the boundary bin bstar is known:
@@ -1954,7 +1983,7 @@ __device__ __noinline__ int32_t rwide_row(const RowCtx& rc, const RowSmem& sm, c
       const int32_t idx = static_cast<int32_t>(~static_cast<uint32_t>(wd));
       if (!kept_by(key, idx, bth.key, bth.idx)) continue;
       const float y = kfloat(key);
-      const uint32_t rk = rc.q ? prace_key(pweight(y, H).wf, __ldg(rc.q + idx), eps) : 0u;
+      const uint32_t rk = rc.race ? prace_key(pweight(y, H).wf, rq1(rc, idx), eps) : 0u;
       const float r = rk ? prace_value(rk, f24b) : -1.0f;
       if (rk && (r > rbest || (r == rbest && idx < ridx))) {
         rbest = r;
@@ -2105,7 +2134,12 @@ __device__ __forceinline__ RowFlags row_setup(const Params& P, int64_t row, cons
   f.topp_on = !f.single && !p_nan && f.p > 0.0f && f.p < 1.0f;
   RowCtx& rc = *rcp;
   rc.x = reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(P.logits) + row * P.V * esize);
-  rc.q = P.q ? P.q + row * P.V : nullptr;  // none: sampling off
+  rc.q = P.q ? P.q + row * P.V : nullptr;  // none: sampling off or generated draws
+  rc.gen = P.gen != 0;
+  rc.race = rc.q != nullptr || rc.gen;
+  rc.seed = P.seed;
+  rc.step = P.step;
+  rc.row = row;
   rc.out = P.need_logits ? P.out_filtered + row * P.V : nullptr;
   rc.V = V;
   rc.nv = V / G;

@@ -123,6 +123,24 @@ kps_status kps_sample(const void* logits, kps_dtype dt, int64_t B, int64_t V,
                       int64_t* out_idx, float* out_filtered,
                       void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * kps_sample_seeded — kps_sample racing with Exp(1) draws the library generates
+ * instead of a caller-supplied q, so no q is read from memory.  The draw of
+ * row b, token v is Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel
+ * Random Numbers: As Easy as 1, 2, 3", SC'11) with key (seed low 32 bits,
+ * seed high 32 bits) on the counter (v / 4, b, step low, step high), output
+ * word v mod 4: u = (2 (w >> 9) + 1) 2^-24 and q = -log(u).  Counter-based:
+ * any row or token can be drawn alone, and results do not depend on the
+ * launch shape.  Change `step` (or `seed`) between decode steps.  Every other
+ * argument, result and error is that of kps_sample.
+ */
+kps_status kps_sample_seeded(const void* logits, kps_dtype dt, int64_t B, int64_t V,
+                             const int32_t* top_k, const float* top_p, const float* temperature,
+                             const int32_t* seen_indptr, const int32_t* seen_ids,
+                             const float* penalty, unsigned long long seed, unsigned long long step,
+                             float eps, int need_logits, int64_t* out_idx, float* out_filtered,
+                             void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* Reads (and clears) the device status word of a workspace: waits for the
  * stream, stores KPS_OK or the first device-side error code in *out. */
 kps_status kps_last_device_status(void* workspace, cudaStream_t stream, int* out);

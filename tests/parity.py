@@ -21,7 +21,7 @@ def to_dev(a, dev):
     return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
 
-def run_gpu(inp, dev="cuda:0", need_logits=None, workspace=None, stream=None):
+def run_gpu(inp, dev="cuda:0", need_logits=None, workspace=None, stream=None, seed=None, step=0):
     import torch
     import decode_token_sampling_gb300 as kps
 
@@ -35,7 +35,8 @@ def run_gpu(inp, dev="cuda:0", need_logits=None, workspace=None, stream=None):
         kw = dict(seen_indptr=to_dev(inp.seen_indptr, dev), seen_ids=to_dev(inp.seen_ids, dev),
                   penalty=to_dev(inp.penalty, dev))
     idx, filt = kps.sample(logits, to_dev(inp.top_k, dev), to_dev(inp.top_p, dev), to_dev(inp.temperature, dev),
-                           to_dev(inp.q, dev) if inp.q is not None else None, eps=inp.eps, need_logits=nl, workspace=workspace, stream=stream,
+                           to_dev(inp.q, dev) if (inp.q is not None and seed is None) else None, eps=inp.eps,
+                           seed=seed, step=step, need_logits=nl, workspace=workspace, stream=stream,
                            **kw)
     torch.cuda.synchronize()
     return idx.cpu().numpy(), (filt.cpu().numpy() if filt is not None else None)

@@ -263,3 +263,26 @@ def test_sampling_off_edge_rows():
     ref = oracle.sample(inp)
     gi, gf = run_gpu(inp)
     compare(inp, ref, gi, gf, "edge rows [sampling off]")
+
+
+@pytest.mark.parametrize("name", WORKLOADS)
+def test_generated_draws(name, kernel):
+    """kps_sample_seeded: the race with the library's own Philox4x32-10 Exp(1) draws matches
+    the oracle racing with the same draws (generated on the CPU from their definition)."""
+    seed, step = 0x5EED0000 + WORKLOADS.index(name), 11
+    inp = make_workload(name)
+    inp.q = oracle.exp_draws(inp.B, inp.V, seed, step)
+    ref = oracle.sample(inp)
+    gi, gf = run_gpu(inp, seed=seed, step=step)
+    compare(inp, ref, gi, gf, f"{name} [generated draws]")
+
+
+def test_generated_draws_edge_rows():
+    """Generated draws on rows with NaN/-inf logits, ties, penalties and edge parameters, and
+    another step of the same seed."""
+    inp = make_random(24, 5004, seed=93, ties=True, special=True, penalty=1.5, n_seen=50)
+    for step in (0, 2**40 + 3):
+        inp.q = oracle.exp_draws(inp.B, inp.V, 77, step)
+        ref = oracle.sample(inp)
+        gi, gf = run_gpu(inp, seed=77, step=step)
+        compare(inp, ref, gi, gf, f"edge rows [generated draws, step {step}]")
