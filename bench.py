@@ -218,6 +218,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--draws", default="supplied", choices=["supplied", "generated", "off"],
+                    help="the race's Exp(1) draws: the workload's q (the metric's definition), generated in "
+                         "the kernel from a seed (kps_sample_seeded), or sampling off (no race)")
     ap.add_argument("--kernel", default="auto", choices=["auto", "cluster", "row"],
                     help="kernel policy (auto picks per shape; both compute the same results)")
     args = ap.parse_args()
@@ -260,8 +263,12 @@ def main():
     wsp = kps.new_workspace(B, V, logits.dtype, dev)
     stream = torch.cuda.Stream(dev)
 
+    q_arg = q if args.draws == "supplied" else None
+    seed_arg = 0x5EED0003 if args.draws == "generated" else None
+
     def step():
-        kps.sample(logits, top_k, top_p, temp, q, eps=inp.eps, need_logits=inp.need_logits, out_idx=out_idx,
+        kps.sample(logits, top_k, top_p, temp, q_arg, seed=seed_arg, step=7, eps=inp.eps, need_logits=inp.need_logits,
+                   out_idx=out_idx,
                    out_filtered=out_f, workspace=wsp, stream=stream, **pen_kw)
 
     with torch.cuda.stream(stream):
@@ -313,13 +320,15 @@ def main():
     if out_f is not None:
         kept = (out_f != float("-inf")).sum(dim=1).to(torch.int64)
     else:
-        _, f_tmp = kps.sample(logits, top_k, top_p, temp, q, eps=inp.eps, need_logits=True, workspace=wsp, **pen_kw)
+        _, f_tmp = kps.sample(logits, top_k, top_p, temp, q_arg, seed=seed_arg, step=7, eps=inp.eps, need_logits=True,
+                              workspace=wsp, **pen_kw)
         kept = (f_tmp != float("-inf")).sum(dim=1).to(torch.int64)
         del f_tmp
     nnz = int(inp.seen_ids.size) if inp.seen_ids is not None else 0
-    alg_bytes = (B * V * esize + (B * V * 4 if inp.need_logits else 0) + int(kept.sum().item()) * 4 + nnz * 4
+    q_kept = int(kept.sum().item()) * 4 if args.draws == "supplied" else 0  # q read at the kept indices
+    alg_bytes = (B * V * esize + (B * V * 4 if inp.need_logits else 0) + q_kept + nnz * 4
                  + B * (4 * 4 + 8 + (4 if pen_kw else 0)))
-    metric_bytes = inp.metric_bytes()
+    metric_bytes = inp.metric_bytes() - (0 if args.draws == "supplied" else B * V * 4)  # no q without supplied draws
     peaks = measured_peaks()
     achieved_gbs = alg_bytes / (kernel_ms / 1e3) / 1e9
     traffic = ncu_traffic_per_launch(kernel_name, args.workload)
@@ -334,19 +343,22 @@ def main():
     d_logits, d_q = torch.empty_like(logits), torch.empty_like(q)
     d_k, d_p, d_t = torch.empty_like(top_k), torch.empty_like(top_p), torch.empty_like(temp)
     d_pen = {k: torch.empty_like(v) for k, v in pen_kw.items()}
-    h2d = sum(x.numel() * x.element_size() for x in [h_logits, h_q, h_k, h_p, h_t, *h_pen.values()])
+    h_in = [h_logits, h_k, h_p, h_t, *h_pen.values()] + ([h_q] if args.draws == "supplied" else [])
+    h2d = sum(x.numel() * x.element_size() for x in h_in)
     d2h = h_idx.numel() * 8 + (h_out.numel() * 4 if h_out is not None else 0)
 
     def e2e_step():
         with torch.cuda.stream(stream):
             d_logits.view(torch.int16 if inp.dtype == "bf16" else torch.float32).copy_(h_logits, non_blocking=True)
-            d_q.copy_(h_q, non_blocking=True)
+            if args.draws == "supplied":
+                d_q.copy_(h_q, non_blocking=True)
             d_k.copy_(h_k, non_blocking=True)
             d_p.copy_(h_p, non_blocking=True)
             d_t.copy_(h_t, non_blocking=True)
             for k_, v_ in d_pen.items():
                 v_.copy_(h_pen[k_], non_blocking=True)
-            kps.sample(d_logits, d_k, d_p, d_t, d_q, eps=inp.eps, need_logits=inp.need_logits, out_idx=out_idx,
+            kps.sample(d_logits, d_k, d_p, d_t, d_q if args.draws == "supplied" else None, seed=seed_arg, step=7,
+                       eps=inp.eps, need_logits=inp.need_logits, out_idx=out_idx,
                        out_filtered=out_f, workspace=wsp, stream=stream, **d_pen)
             h_idx.copy_(out_idx, non_blocking=True)
             if h_out is not None:
@@ -374,7 +386,7 @@ def main():
         "metric": metric_name(args.workload), "value": rows_per_s, "unit": "rows/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": inp.dtype, "data": "synthetic (seeded, see workloads.py)",
-        "config": workload_config(args.workload),
+        "config": dict(workload_config(args.workload), **({} if args.draws == "supplied" else {"draws": args.draws})),
         "tokens_per_s": rows_per_s,
         "metric_gbs": metric_bytes / (ms_per_step / 1e3) / 1e9,
         "metric_pct_of_8tbs": 100.0 * metric_bytes / (ms_per_step / 1e3) / 1e9 / NOMINAL_HBM_GBS,
