@@ -32,6 +32,13 @@ class KpsError(RuntimeError):
 _lib: Optional[ctypes.CDLL] = None
 
 
+class StepOpts(ctypes.Structure):
+    """kps_step_opts (include/kps.h)."""
+    _fields_ = [("q", ctypes.c_void_p), ("generate", ctypes.c_int), ("seed", ctypes.c_uint64),
+                ("step", ctypes.c_uint64), ("finished", ctypes.c_void_p), ("eos_id", ctypes.c_int64),
+                ("unfinished", ctypes.c_void_p)]
+
+
 def load_library() -> ctypes.CDLL:
     """Load libkps.so (raises if it has not been built)."""
     global _lib
@@ -54,6 +61,9 @@ def load_library() -> ctypes.CDLL:
     lib.kps_sample_seeded.restype = I32
     lib.kps_sample_seeded.argtypes = [P, I32, I64, I64, P, P, P, P, P, P, ctypes.c_uint64, ctypes.c_uint64,
                                       ctypes.c_float, I32, P, P, P, ctypes.c_size_t, P]
+    lib.kps_sample_step.restype = I32
+    lib.kps_sample_step.argtypes = [P, I32, I64, I64, P, P, P, P, P, P, ctypes.POINTER(StepOpts), ctypes.c_float,
+                                    I32, P, P, P, ctypes.c_size_t, P]
     lib.kps_set_kernel_policy.restype = I32
     lib.kps_set_kernel_policy.argtypes = [I32]
     lib.kps_get_kernel_policy.restype = I32
@@ -149,13 +159,16 @@ def sample(logits: torch.Tensor, top_k: torch.Tensor, top_p: torch.Tensor, tempe
            penalty: Optional[torch.Tensor] = None, eps: float = 1e-20, need_logits: bool = False,
            out_idx: Optional[torch.Tensor] = None, out_filtered: Optional[torch.Tensor] = None,
            workspace: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None,
-           seed: Optional[int] = None, step: int = 0):
+           seed: Optional[int] = None, step: int = 0, finished: Optional[torch.Tensor] = None,
+           eos_id: int = 0, unfinished: Optional[torch.Tensor] = None):
     """One fused sampling step on the GPU (asynchronous on `stream`).
 
     q: the race's Exp(1) draws [B, V] fp32, or None to sample off (each row's index is
     the first element of its kept set's order: the argmax of the filtered row).
     seed: race with draws generated from (seed, step) instead (q must then be None;
     kps_sample_seeded in include/kps.h defines them).
+    finished (uint8 [B], updated in place), eos_id, unfinished (int32 [1]): the
+    end-of-sequence epilogue of kps_sample_step.
     Returns (out_idx int64[B], out_filtered float32[B,V] or None).
     """
     lib = load_library()
@@ -192,7 +205,18 @@ def sample(logits: torch.Tensor, top_k: torch.Tensor, top_p: torch.Tensor, tempe
     if workspace is None:
         workspace = new_workspace(B, V, logits.dtype, dev)
     s = stream if stream is not None else torch.cuda.current_stream(dev)
-    if seed is not None:
+    if finished is not None:
+        _check(finished, "finished", torch.uint8, (B,), dev)
+        if unfinished is not None:
+            _check(unfinished, "unfinished", torch.int32, (1,), dev)
+        opts = StepOpts(_ptr(q) if seed is None else None, 0 if seed is None else 1,
+                        0 if seed is None else int(seed) & (2**64 - 1), int(step) & (2**64 - 1), _ptr(finished),
+                        int(eos_id), _ptr(unfinished))
+        st = lib.kps_sample_step(_ptr(logits), dt, B, V, _ptr(top_k), _ptr(top_p), _ptr(temperature),
+                                 _ptr(seen_indptr), _ptr(seen_ids), _ptr(penalty), ctypes.byref(opts), float(eps),
+                                 1 if need_logits else 0, _ptr(out_idx), _ptr(out_filtered), _ptr(workspace),
+                                 workspace.numel(), ctypes.c_void_p(s.cuda_stream))
+    elif seed is not None:
         st = lib.kps_sample_seeded(_ptr(logits), dt, B, V, _ptr(top_k), _ptr(top_p), _ptr(temperature),
                                    _ptr(seen_indptr), _ptr(seen_ids), _ptr(penalty), int(seed) & (2**64 - 1),
                                    int(step) & (2**64 - 1), float(eps), 1 if need_logits else 0, _ptr(out_idx),
@@ -204,7 +228,8 @@ def sample(logits: torch.Tensor, top_k: torch.Tensor, top_p: torch.Tensor, tempe
                             1 if need_logits else 0, _ptr(out_idx), _ptr(out_filtered), _ptr(workspace),
                             workspace.numel(), ctypes.c_void_p(s.cuda_stream))
     if st != 0:
-        raise KpsError(st, "kps_sample_seeded" if seed is not None else "kps_sample")
+        raise KpsError(st, "kps_sample_step" if finished is not None else
+                       "kps_sample_seeded" if seed is not None else "kps_sample")
     return out_idx, out_filtered
 
 

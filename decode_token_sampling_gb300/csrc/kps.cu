@@ -120,6 +120,9 @@ struct Params {
   int pre_rows;        // records available (the first pre_rows top-p-only rows use them)
   int gen;             // race with generated Exp(1) draws (q is then nullptr)
   unsigned long long seed, step;  // their generator's key and the decode step
+  unsigned char* finished;        // [B] end-of-sequence flags (nullptr: no epilogue)
+  long long eos;                  // the end-of-sequence token
+  int* unfinished;                // rows still unfinished after the step (nullptr: not counted)
 };
 
 constexpr int kMaxRowList = 256;  // rows one worker (CTA or cluster) may own in a filtered launch
@@ -261,6 +264,19 @@ __device__ __forceinline__ float gen_q1(unsigned long long seed, unsigned long l
                                 static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
   const int e = static_cast<int>(v & 3);
   return exp_of_word(e == 0 ? w.x : e == 1 ? w.y : e == 2 ? w.z : w.w);
+}
+
+// The end-of-sequence epilogue of a row's chosen token (MiniMind, "Chapter 10: inference
+// generation", the generate loop): a finished row emits the end-of-sequence token, a row
+// that emits it becomes finished, and the rows left unfinished are counted.
+__device__ __forceinline__ long long eos_epilogue(const Params& P, int64_t row, int32_t chosen) {
+  if (!P.finished) return chosen;
+  const bool was = P.finished[row] != 0;
+  const long long out = was ? P.eos : static_cast<long long>(chosen);
+  const bool now = was || out == P.eos;
+  if (now && !was) P.finished[row] = 1;
+  if (!now && P.unfinished) atomicAdd(P.unfinished, 1);
+  return out;
 }
 
 __device__ __forceinline__ float softmax_weight(float x, float M) {
@@ -1553,7 +1569,7 @@ __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P)
           if (kept_by(c.cand_key[i], c.cand_idx[i], th.key, th.idx)) orow[c.cand_idx[i] - c0] = kfloat(c.cand_key[i]);
       }
     }
-    if (rank == 0 && threadIdx.x == 0) P.out_idx[row] = chosen;
+    if (rank == 0 && threadIdx.x == 0) P.out_idx[row] = eos_epilogue(P, row, chosen);
 
     // the chunk buffer is free: start the next row's load if it has not started yet
     __syncthreads();
@@ -1899,7 +1915,8 @@ static kps_status sample_impl(const void* logits, kps_dtype dt, int64_t B, int64
                               const int32_t* seen_ids, const float* penalty, const float* q, float eps,
                               int need_logits, int64_t* out_idx, float* out_filtered, void* workspace,
                               size_t workspace_bytes, cudaStream_t stream, int gen, unsigned long long seed,
-                              unsigned long long step) {
+                              unsigned long long step, unsigned char* finished = nullptr, long long eos = 0,
+                              int* unfinished = nullptr) {
   if (dt != KPS_F32 && dt != KPS_BF16) return KPS_ERR_INVALID_ARG;
   if (V < 1 || V > INT32_MAX || B < 0) return KPS_ERR_INVALID_ARG;
   if (!(eps >= 0.0f) || std::isinf(eps)) return KPS_ERR_INVALID_ARG;
@@ -1944,6 +1961,13 @@ static kps_status sample_impl(const void* logits, kps_dtype dt, int64_t B, int64
   P.gen = gen ? 1 : 0;
   P.seed = seed;
   P.step = step;
+  P.finished = finished;
+  P.eos = eos;
+  P.unfinished = finished ? unfinished : nullptr;
+  if (P.unfinished && cudaMemsetAsync(P.unfinished, 0, sizeof(int), stream) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return KPS_ERR_CUDA;
+  }
   P.eps = eps;
   P.need_logits = need_logits ? 1 : 0;
   P.out_idx = out_idx;
@@ -2047,6 +2071,19 @@ kps_status kps_sample_seeded(const void* logits, kps_dtype dt, int64_t B, int64_
                              float* out_filtered, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   return sample_impl(logits, dt, B, V, top_k, top_p, temperature, seen_indptr, seen_ids, penalty, nullptr, eps,
                      need_logits, out_idx, out_filtered, workspace, workspace_bytes, stream, 1, seed, step);
+}
+
+kps_status kps_sample_step(const void* logits, kps_dtype dt, int64_t B, int64_t V, const int32_t* top_k,
+                           const float* top_p, const float* temperature, const int32_t* seen_indptr,
+                           const int32_t* seen_ids, const float* penalty, const kps_step_opts* opts, float eps,
+                           int need_logits, int64_t* out_idx, float* out_filtered, void* workspace,
+                           size_t workspace_bytes, cudaStream_t stream) {
+  if (!opts) return KPS_ERR_INVALID_ARG;
+  if (opts->unfinished && !opts->finished) return KPS_ERR_INVALID_ARG;
+  return sample_impl(logits, dt, B, V, top_k, top_p, temperature, seen_indptr, seen_ids, penalty,
+                     opts->generate ? nullptr : opts->q, eps, need_logits, out_idx, out_filtered, workspace,
+                     workspace_bytes, stream, opts->generate ? 1 : 0, opts->seed, opts->step, opts->finished,
+                     static_cast<long long>(opts->eos_id), opts->unfinished);
 }
 
 kps_status kps_set_kernel_policy(int policy) {

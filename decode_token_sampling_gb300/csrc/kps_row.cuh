@@ -2312,7 +2312,7 @@ __global__ void __launch_bounds__(kRT, 2) kps_row_kernel(const Params P) {
       if (ord >= 0) rec = prec_at(P, ord);
       chosen = rwide_row<kBF16>(rc, sm, tm, f.topp_on, f.p, P.eps, P.exact != 0, ord >= 0 ? &rec : nullptr);
     }
-    if (threadIdx.x == 0 && chosen >= 0) P.out_idx[row] = chosen;
+    if (threadIdx.x == 0 && chosen >= 0) P.out_idx[row] = eos_epilogue(P, row, chosen);
     __syncthreads();
     row_teardown(P, row, f, sm);
   }

@@ -141,6 +141,37 @@ kps_status kps_sample_seeded(const void* logits, kps_dtype dt, int64_t B, int64_
                              float eps, int need_logits, int64_t* out_idx, float* out_filtered,
                              void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * kps_sample_step — one decode step's sampling with every option: the draws
+ * (supplied, generated or none) and the end-of-sequence epilogue of a
+ * generation loop (MiniMind, "Chapter 10: inference generation", the
+ * generate loop: a finished sequence emits the end-of-sequence token, a
+ * sequence that emits it becomes finished, and the loop stops once all are
+ * finished), applied inside the kernel as each row's index is written.
+ */
+typedef struct {
+  const float* q;            /* [B, V] fp32 draws as for kps_sample, or NULL
+                                (sampling off) — ignored when generate != 0 */
+  int generate;              /* non-zero: draws generated from (seed, step) as
+                                for kps_sample_seeded */
+  unsigned long long seed, step;
+  unsigned char* finished;   /* [B] device flags, read and updated (0 or 1), or
+                                NULL: no epilogue.  A row flagged finished
+                                emits eos_id (its filtered row is still
+                                written); a row that emits eos_id is flagged. */
+  int64_t eos_id;            /* the end-of-sequence token */
+  int* unfinished;           /* device int, or NULL: set to the number of rows
+                                left unfinished after the step (0: the loop can
+                                stop).  Requires finished. */
+} kps_step_opts;
+
+kps_status kps_sample_step(const void* logits, kps_dtype dt, int64_t B, int64_t V,
+                           const int32_t* top_k, const float* top_p, const float* temperature,
+                           const int32_t* seen_indptr, const int32_t* seen_ids,
+                           const float* penalty, const kps_step_opts* opts, float eps,
+                           int need_logits, int64_t* out_idx, float* out_filtered,
+                           void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* Reads (and clears) the device status word of a workspace: waits for the
  * stream, stores KPS_OK or the first device-side error code in *out. */
 kps_status kps_last_device_status(void* workspace, cudaStream_t stream, int* out);

@@ -43,6 +43,8 @@ def _load() -> ctypes.CDLL:
         lib.kpso_sample.restype = ctypes.c_int
         lib.kpso_sample.argtypes = [P, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, P, P, P, P, P, P,
                                     P, ctypes.c_float, ctypes.c_int, P, P, P, P, P]
+        lib.kpso_eos_epilogue.restype = ctypes.c_int64
+        lib.kpso_eos_epilogue.argtypes = [P, P, ctypes.c_int64, ctypes.c_int64]
         lib.kpso_exp_draws.restype = ctypes.c_int
         lib.kpso_exp_draws.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_uint64, ctypes.c_uint64, P]
         lib.kpso_philox4x32_10.restype = None
@@ -111,4 +113,11 @@ def philox4x32_10(counter, key) -> list:
     c = np.array(counter, dtype=np.uint32)
     _load().kpso_philox4x32_10(c.ctypes.data_as(ctypes.c_void_p), int(key[0]), int(key[1]))
     return [int(x) for x in c]
+
+
+def eos_epilogue(idx: np.ndarray, finished: np.ndarray, eos: int) -> int:
+    """The end-of-sequence epilogue on host arrays (int64 idx, uint8 finished, both updated
+    in place); returns the rows left unfinished."""
+    assert idx.dtype == np.int64 and finished.dtype == np.uint8 and idx.shape == finished.shape
+    return int(_load().kpso_eos_epilogue(_ptr(idx), _ptr(finished), int(eos), idx.size))
 

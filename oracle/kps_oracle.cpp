@@ -274,4 +274,18 @@ int kpso_exp_draws(int64_t B, int64_t V, uint64_t seed, uint64_t step, float* q)
   return 0;
 }
 
+// The end-of-sequence epilogue of a decode step [MM10 generate loop: a finished sequence
+// emits eos_token_id (torch.where on the finished flags), then finished |= the token
+// equals eos_token_id, and the loop stops once every sequence is finished].  Updates idx
+// and finished in place; returns the number of rows left unfinished.
+int64_t kpso_eos_epilogue(int64_t* idx, uint8_t* finished, int64_t eos, int64_t B) {
+  int64_t left = 0;
+  for (int64_t b = 0; b < B; ++b) {
+    if (finished[b]) idx[b] = eos;
+    if (idx[b] == eos) finished[b] = 1;
+    if (!finished[b]) ++left;
+  }
+  return left;
+}
+
 }  // extern "C"

@@ -80,3 +80,17 @@ def test_no_silent_cpu_path(lib):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert _call(lib) == 4
+
+
+def test_step_options_are_checked_without_gpu(lib):
+    fake = ctypes.c_void_p(1 << 20)
+    lib.kps_sample_step.restype = ctypes.c_int
+    args = [fake, 0, 4, 100, fake, fake, fake, None, None, None, None, ctypes.c_float(1e-20), 0, fake, None,
+            ctypes.c_void_p(1 << 20), ctypes.c_size_t(256), None]
+    assert lib.kps_sample_step(*args) == 1  # no options
+
+    from decode_token_sampling_gb300 import StepOpts
+    o = StepOpts(None, 0, 0, 0, None, 2, fake)  # a count without flags
+    args[10] = ctypes.byref(o)
+    assert lib.kps_sample_step(*args) == 1
+

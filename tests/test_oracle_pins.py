@@ -437,3 +437,17 @@ def test_exp_draws_are_exp1():
     assert abs(x.mean() - 1.0) < 5e-3 and abs(x.var() - 1.0) < 1e-2
     assert abs(np.corrcoef(q[:, :-1].ravel(), q[:, 1:].ravel())[0, 1]) < 5e-3
     assert abs(np.corrcoef(q[:-1].ravel(), q[1:].ravel())[0, 1]) < 5e-3
+
+
+def test_eos_epilogue_follows_the_generate_loop():
+    """MiniMind's generate loop: a finished sequence emits eos, a sequence that emits eos is
+    finished, and the loop may stop when none is left."""
+    idx = np.array([5, 2, 7, 2, 9], np.int64)
+    fin = np.array([0, 0, 1, 0, 1], np.uint8)
+    left = oracle.eos_epilogue(idx, fin, 2)
+    assert idx.tolist() == [5, 2, 2, 2, 2]
+    assert fin.tolist() == [0, 1, 1, 1, 1]
+    assert left == 1
+    idx = np.array([2, 2], np.int64)
+    fin = np.zeros(2, np.uint8)
+    assert oracle.eos_epilogue(idx, fin, 2) == 0 and fin.tolist() == [1, 1]

@@ -286,3 +286,39 @@ def test_generated_draws_edge_rows():
         ref = oracle.sample(inp)
         gi, gf = run_gpu(inp, seed=77, step=step)
         compare(inp, ref, gi, gf, f"edge rows [generated draws, step {step}]")
+
+
+@pytest.mark.parametrize("draws", ["supplied", "generated"])
+def test_eos_epilogue(kernel, draws):
+    """kps_sample_step's end-of-sequence epilogue: finished rows emit eos, rows that emit it
+    become finished, and the unfinished rows are counted, as the oracle's epilogue does."""
+    import torch
+    import decode_token_sampling_gb300 as kps
+    inp = make_workload("batch256_penalty", rows=range(0, 256, 3))
+    seed = 4242
+    if draws == "generated":
+        inp.q = oracle.exp_draws(inp.B, inp.V, seed, 3)
+    ref = oracle.sample(inp)
+    rng = np.random.default_rng(5)
+    fin0 = (rng.random(inp.B) < 0.3).astype(np.uint8)
+    eos = int(ref["idx"][np.nonzero(fin0 == 0)[0][0]])  # an unfinished row emits eos
+    ref_idx, ref_fin = ref["idx"].copy(), fin0.copy()
+    left = oracle.eos_epilogue(ref_idx, ref_fin, eos)
+    dev = "cuda:0"
+    fin = torch.from_numpy(fin0.copy()).to(dev)
+    unf = torch.full((1,), -5, dtype=torch.int32, device=dev)
+    kw = dict(seen_indptr=torch.from_numpy(inp.seen_indptr).to(dev), seen_ids=torch.from_numpy(inp.seen_ids).to(dev),
+              penalty=torch.from_numpy(inp.penalty).to(dev))
+    idx, filt = kps.sample(torch.from_numpy(inp.logits).to(dev), torch.from_numpy(inp.top_k).to(dev),
+                           torch.from_numpy(inp.top_p).to(dev), torch.from_numpy(inp.temperature).to(dev),
+                           torch.from_numpy(inp.q).to(dev) if draws == "supplied" else None,
+                           seed=seed if draws == "generated" else None, step=3, eps=inp.eps, need_logits=True,
+                           finished=fin, eos_id=eos, unfinished=unf, **kw)
+    torch.cuda.synchronize()
+    near = (ref["race_gap"] < 1e-6) | (ref["topp_gap"] < 1e-6)
+    got = idx.cpu().numpy()
+    ok = (got == ref_idx) | near
+    assert ok.all(), np.nonzero(~ok)[0][:10]
+    assert np.array_equal(fin.cpu().numpy(), ref_fin) or near.any()
+    assert int(unf.item()) == left or near.any()
+    assert (got[fin0 == 1] == eos).all()
