@@ -1377,14 +1377,17 @@ __device__ __forceinline__ void sh_max_word(uint32_t a, uint32_t key, unsigned l
 // (h[b], h[kRPBins + b]: a bin takes any row of at most 2^18 elements without overflow),
 // and per bin the best race word (race key, index; the lower index on equal keys) in
 // ub[b].  Returns the part's largest value as a key.
-template <bool kBF16, bool kGen>
+// kDraw: 0 q loaded, 1 q generated, 2 sampling off (the per-bin word is then the bin's
+// first element of the order: its value key and index).
+template <bool kBF16, int kDraw>
 __device__ __noinline__ unsigned long long rp_pass_a_t(const RowCtx& rc, float H, float eps, uint32_t* h,
                                                        unsigned long long* ub, unsigned long long* red) {
   constexpr int G = kBF16 ? 8 : 4;
   constexpr int kUA = kBF16 ? 1 : 2;  // vectors in flight per thread (q rides along)
   const unsigned long long pol = l2_policy_last();
   const uint4* xr = rc.x;
-  const bool race = rc.race;  // sampling off: no race words
+  constexpr bool kGen = kDraw == 1;
+  const bool race = kDraw != 2;
   const float4* qr = reinterpret_cast<const float4*>(rc.q);
   const unsigned long long seed = rc.seed, step = rc.step;
   const int64_t row = rc.row;
@@ -1434,10 +1437,8 @@ __device__ __noinline__ unsigned long long rp_pass_a_t(const RowCtx& rc, float H
           sh_red_add(&h[kRPBins + pw.b], pw.w24 >> 12);
           const float4 q4 = qv[u][e / 4];
           const float qe = (e & 3) == 0 ? q4.x : (e & 3) == 1 ? q4.y : (e & 3) == 2 ? q4.z : q4.w;
-          if (race) {
-            const uint32_t key = prace_key(pw.wf, qe, eps);
-            sh_max_word(smem_u32(ub + pw.b), key, order_word(key, g * G + e));
-          }
+          const uint32_t key = kDraw == 2 ? fkey(y) : prace_key(pw.wf, qe, eps);
+          sh_max_word(smem_u32(ub + pw.b), key, order_word(key, g * G + e));
         }
       }
     }
@@ -1451,7 +1452,8 @@ __device__ __noinline__ unsigned long long rp_pass_a_t(const RowCtx& rc, float H
 template <bool kBF16>
 __device__ __forceinline__ unsigned long long rp_pass_a(const RowCtx& rc, float H, float eps, uint32_t* h,
                                                         unsigned long long* ub, unsigned long long* red) {
-  return rc.gen ? rp_pass_a_t<kBF16, true>(rc, H, eps, h, ub, red) : rp_pass_a_t<kBF16, false>(rc, H, eps, h, ub, red);
+  return rc.gen ? rp_pass_a_t<kBF16, 1>(rc, H, eps, h, ub, red)
+                : rc.race ? rp_pass_a_t<kBF16, 0>(rc, H, eps, h, ub, red) : rp_pass_a_t<kBF16, 2>(rc, H, eps, h, ub, red);
 }
 
 // Pass B of top-p-only rows over this CTA's part, once the boundary bin bstar is known:
@@ -1757,8 +1759,11 @@ __device__ __noinline__ int32_t rwide_row(const RowCtx& rc, const RowSmem& sm, c
     for (int e = 0; e < kRPBins / kRT; ++e) {
       const int b = (kRPBins / kRT) * static_cast<int>(threadIdx.x) + e;
       if (b < bstar && ubest[e]) {
-        const float rv = prace_value(static_cast<uint32_t>(ubest[e] >> 32), __fmul_rn(ftab[b], 5.9604644775390625e-8f));
-        const unsigned long long c = order_word(fkey(rv), static_cast<int32_t>(~static_cast<uint32_t>(ubest[e])));
+        unsigned long long c = ubest[e];  // sampling off: already the bin's first element of the order
+        if (rc.race) {
+          const float rv = prace_value(static_cast<uint32_t>(ubest[e] >> 32), __fmul_rn(ftab[b], 5.9604644775390625e-8f));
+          c = order_word(fkey(rv), static_cast<int32_t>(~static_cast<uint32_t>(ubest[e])));
+        }
         rb = c > rb ? c : rb;
       }
     }
@@ -1977,11 +1982,13 @@ __device__ __noinline__ int32_t rwide_row(const RowCtx& rc, const RowSmem& sm, c
     const float f24b = __fmul_rn(fbf, 5.9604644775390625e-8f);
     float rbest = -1.0f;
     int ridx = INT_MAX;
+    unsigned long long gfirst = 0;  // sampling off: the first kept entry of the order
     for (int i = threadIdx.x; i < total; i += kRT) {
       const unsigned long long wd = sm.cw[i];
       const uint32_t key = static_cast<uint32_t>(wd >> 32);
       const int32_t idx = static_cast<int32_t>(~static_cast<uint32_t>(wd));
       if (!kept_by(key, idx, bth.key, bth.idx)) continue;
+      gfirst = wd > gfirst ? wd : gfirst;
       const float y = kfloat(key);
       const uint32_t rk = rc.race ? prace_key(pweight(y, H).wf, rq1(rc, idx), eps) : 0u;
       const float r = rk ? prace_value(rk, f24b) : -1.0f;
@@ -1991,7 +1998,7 @@ __device__ __noinline__ int32_t rwide_row(const RowCtx& rc, const RowSmem& sm, c
       }
       if (rc.out) rc.out[idx] = y;
     }
-    unsigned long long c = rbest >= 0.0f ? order_word(fkey(rbest), ridx) : 0ull;
+    unsigned long long c = !rc.race ? gfirst : rbest >= 0.0f ? order_word(fkey(rbest), ridx) : 0ull;
     c = c > rb ? c : rb;
     unsigned long long dummy = 0;
     rblock_max2(c, dummy, sm.red);
