@@ -49,6 +49,10 @@ def _load() -> ctypes.CDLL:
         lib.kpso_exp_draws.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_uint64, ctypes.c_uint64, P]
         lib.kpso_philox4x32_10.restype = None
         lib.kpso_philox4x32_10.argtypes = [P, ctypes.c_uint32, ctypes.c_uint32]
+        lib.kpso_seen_ids_from_bits.restype = ctypes.c_int64
+        lib.kpso_seen_ids_from_bits.argtypes = [P, ctypes.c_int64, ctypes.c_int64, P, P]
+        lib.kpso_seen_append.restype = None
+        lib.kpso_seen_append.argtypes = [P, P, ctypes.c_int64, ctypes.c_int64]
         _lib = lib
     return _lib
 
@@ -120,4 +124,25 @@ def eos_epilogue(idx: np.ndarray, finished: np.ndarray, eos: int) -> int:
     in place); returns the rows left unfinished."""
     assert idx.dtype == np.int64 and finished.dtype == np.uint8 and idx.shape == finished.shape
     return int(_load().kpso_eos_epilogue(_ptr(idx), _ptr(finished), int(eos), idx.size))
+
+
+def seen_ids_from_bits(bits: np.ndarray, V: int):
+    """The seen sets of a uint32 bit matrix [B, ceil(V/32)] as CSR (indptr int32 [B+1],
+    ids int32 [nnz], each row's ids distinct and ascending)."""
+    bits = np.ascontiguousarray(bits).view(np.uint32)
+    B = bits.shape[0]
+    assert bits.shape == (B, (V + 31) // 32)
+    indptr = np.zeros(B + 1, np.int32)
+    lib = _load()
+    n = int(lib.kpso_seen_ids_from_bits(_ptr(bits), B, V, _ptr(indptr), None))
+    ids = np.zeros(max(n, 1), np.int32)
+    lib.kpso_seen_ids_from_bits(_ptr(bits), B, V, _ptr(indptr), _ptr(ids))
+    return indptr, ids[:n]
+
+
+def seen_append(bits: np.ndarray, idx: np.ndarray, V: int) -> None:
+    """Sets the bit of each row's token idx[b] (int64, ignored outside [0, V)) in place."""
+    assert bits.dtype in (np.uint32, np.int32) and bits.flags.c_contiguous and idx.dtype == np.int64
+    assert bits.shape == (idx.size, (V + 31) // 32)
+    _load().kpso_seen_append(_ptr(bits), _ptr(idx), idx.size, V)
 

@@ -288,4 +288,34 @@ int64_t kpso_eos_epilogue(int64_t* idx, uint8_t* finished, int64_t eos, int64_t 
   return left;
 }
 
+// The seen set of each row as the sorted list of distinct ids [MM10 §10.7: the penalty
+// runs over the unique ids of the sequence so far], read from its bit form: bit v % 32
+// of word b * W + v / 32 (W = ceil(V / 32)) marks token v of row b; bits of tokens >= V
+// are not ids.  indptr [B + 1] always; ids (room for indptr[B]) when non-NULL.  Returns
+// the number of ids.
+int64_t kpso_seen_ids_from_bits(const uint32_t* bits, int64_t B, int64_t V, int32_t* indptr, int32_t* ids) {
+  const int64_t W = (V + 31) / 32;
+  int64_t n = 0;
+  indptr[0] = 0;
+  for (int64_t b = 0; b < B; ++b) {
+    for (int64_t v = 0; v < V; ++v) {
+      if ((bits[b * W + v / 32] >> (v % 32)) & 1u) {
+        if (ids) ids[n] = static_cast<int32_t>(v);
+        ++n;
+      }
+    }
+    indptr[b + 1] = static_cast<int32_t>(n);
+  }
+  return n;
+}
+
+// One decode step's growth of the seen sets [MM10 generate loop: the step's token is
+// appended to each sequence, so the next step's unique ids are the old ones plus that
+// token]: the bit of idx[b] is set in row b when 0 <= idx[b] < V.
+void kpso_seen_append(uint32_t* bits, const int64_t* idx, int64_t B, int64_t V) {
+  const int64_t W = (V + 31) / 32;
+  for (int64_t b = 0; b < B; ++b)
+    if (idx[b] >= 0 && idx[b] < V) bits[b * W + idx[b] / 32] |= 1u << (idx[b] % 32);
+}
+
 }  // extern "C"

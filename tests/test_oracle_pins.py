@@ -451,3 +451,93 @@ def test_eos_epilogue_follows_the_generate_loop():
     idx = np.array([2, 2], np.int64)
     fin = np.zeros(2, np.uint8)
     assert oracle.eos_epilogue(idx, fin, 2) == 0 and fin.tolist() == [1, 1]
+
+
+# ----------------------------------------------------------------------------------------------
+# The seen set kept as bits across decode steps (MiniMind ch.10: the repetition penalty runs
+# over the unique ids of the sequence so far; the generate loop appends each step's token)
+# ----------------------------------------------------------------------------------------------
+
+def _bits_of(sets, V, junk_rng=None):
+    """Bit matrix of Python id sets (plus, when junk_rng is given, random bits above V)."""
+    W = (V + 31) // 32
+    bits = np.zeros((len(sets), W), np.uint32)
+    for b, s in enumerate(sets):
+        for v in s:
+            bits[b, v // 32] |= np.uint32(1 << (v % 32))
+        if junk_rng is not None and V % 32:
+            bits[b, W - 1] |= np.uint32(int(junk_rng.integers(1, 2**32)) & ~((1 << (V % 32)) - 1) & 0xFFFFFFFF)
+    return bits
+
+
+def test_seen_ids_from_bits_lists_each_set_once():
+    rng = np.random.default_rng(77)
+    V = 70  # three words; bits 70..95 of the last one are not tokens
+    sets = [set(), {0}, {69}, set(int(v) for v in rng.integers(0, V, 40)), set(range(V))]
+    bits = _bits_of(sets, V, junk_rng=rng)
+    indptr, ids = oracle.seen_ids_from_bits(bits, V)
+    assert indptr[0] == 0 and indptr.shape == (len(sets) + 1,)
+    for b, s in enumerate(sets):
+        assert ids[indptr[b]:indptr[b + 1]].tolist() == sorted(s)
+
+
+def test_seen_append_adds_the_token_only():
+    V = 70
+    sets = [{1, 2}, set(), {40}, {5}, {6}]
+    bits = _bits_of(sets, V)
+    idx = np.array([3, 69, 40, -1, V], np.int64)  # in range, top token, already seen, outside x2
+    oracle.seen_append(bits, idx, V)
+    indptr, ids = oracle.seen_ids_from_bits(bits, V)
+    want = [{1, 2, 3}, {69}, {40}, {5}, {6}]
+    for b, s in enumerate(want):
+        assert ids[indptr[b]:indptr[b + 1]].tolist() == sorted(s)
+
+
+def test_penalty_over_bits_equals_penalty_over_the_id_list():
+    """The penalty depends on the set alone: a list with duplicates and out-of-range ids and the
+    bit form of its distinct in-range ids give the same result."""
+    rng = np.random.default_rng(78)
+    B, V = 6, 300
+    x = rng.normal(0, 2, (B, V)).astype(np.float32)
+    lists = [list(rng.integers(-5, V + 5, 60)) + [7, 7, 7] for _ in range(B)]
+    indptr = np.cumsum([0] + [len(l) for l in lists]).astype(np.int32)
+    ids = np.concatenate(lists).astype(np.int32)
+    pen = np.full(B, 1.3, np.float32)
+    kw = dict(top_k=np.array([0, 5, 50, 0, 1, 1025], np.int32), top_p=np.array([1.0, 0.9, 0.7, 0.5, 1.0, 0.95],
+              np.float32), temperature=np.array([1.0, 0.8, 1.2, 0.7, 1.0, 0.9], np.float32))
+    q = oracle.exp_draws(B, V, 5, 0)
+    a = oracle.sample_arrays(x, "f32", kw["top_k"], kw["top_p"], kw["temperature"], q, 1e-20, True, indptr, ids, pen)
+    bits = _bits_of([set(int(v) for v in l if 0 <= v < V) for l in lists], V, junk_rng=rng)
+    ip2, ids2 = oracle.seen_ids_from_bits(bits, V)
+    b = oracle.sample_arrays(x, "f32", kw["top_k"], kw["top_p"], kw["temperature"], q, 1e-20, True, ip2, ids2, pen)
+    np.testing.assert_array_equal(a["idx"], b["idx"])
+    np.testing.assert_array_equal(a["filtered"], b["filtered"])
+
+
+def test_incremental_bits_follow_the_generate_loop():
+    """Three decode steps: the bits grown by seen_append give the penalty over the unique ids
+    of the growing sequence (prompt ids plus every emitted token), built here from a list."""
+    rng = np.random.default_rng(79)
+    B, V = 5, 200
+    seqs = [list(int(v) for v in rng.integers(0, V, 8)) for _ in range(B)]
+    bits = _bits_of([set(s) for s in seqs], V)
+    pen = np.full(B, 1.5, np.float32)
+    top_k = np.array([0, 20, 3, 0, 50], np.int32)
+    top_p = np.array([0.9, 1.0, 0.8, 1.0, 0.6], np.float32)
+    T = np.ones(B, np.float32)
+    for step in range(3):
+        x = rng.normal(0, 1, (B, V)).astype(np.float32)
+        q = oracle.exp_draws(B, V, 11, step)
+        indptr = np.cumsum([0] + [len(s) for s in seqs]).astype(np.int32)
+        ref = oracle.sample_arrays(x, "f32", top_k, top_p, T, q, 1e-20, True, indptr,
+                                   np.concatenate(seqs).astype(np.int32), pen)
+        ip2, ids2 = oracle.seen_ids_from_bits(bits, V)
+        got = oracle.sample_arrays(x, "f32", top_k, top_p, T, q, 1e-20, True, ip2, ids2, pen)
+        np.testing.assert_array_equal(ref["idx"], got["idx"])
+        np.testing.assert_array_equal(ref["filtered"], got["filtered"])
+        for b in range(B):
+            seqs[b].append(int(ref["idx"][b]))
+        oracle.seen_append(bits, got["idx"], V)
+    ip3, ids3 = oracle.seen_ids_from_bits(bits, V)
+    for b in range(B):
+        assert ids3[ip3[b]:ip3[b + 1]].tolist() == sorted(set(seqs[b]))
