@@ -221,6 +221,9 @@ def main():
     ap.add_argument("--draws", default="supplied", choices=["supplied", "generated", "off"],
                     help="the race's Exp(1) draws: the workload's q (the metric's definition), generated in "
                          "the kernel from a seed (kps_sample_seeded), or sampling off (no race)")
+    ap.add_argument("--seen", default="ids", choices=["ids", "bits"],
+                    help="the seen sets: the workload's id lists (CSR, the metric's definition) or a bit matrix "
+                         "kept on the device, the step setting each emitted token's bit (kps_sample_step)")
     ap.add_argument("--kernel", default="auto", choices=["auto", "cluster", "row"],
                     help="kernel policy (auto picks per shape; both compute the same results)")
     args = ap.parse_args()
@@ -256,7 +259,17 @@ def main():
         logits = t(inp.logits)
     top_k, top_p, temp, q = t(inp.top_k), t(inp.top_p), t(inp.temperature), t(inp.q)
     pen_kw = {}
-    if inp.seen_indptr is not None:
+    bits_kw = {}  # device state across steps in the bit form: not an input of each step
+    if inp.seen_indptr is not None and args.seen == "bits":
+        W = (V + 31) // 32
+        hb = np.zeros((B, W), np.uint32)
+        for b in range(B):
+            ids = inp.seen_ids[inp.seen_indptr[b]:inp.seen_indptr[b + 1]]
+            ids = ids[(ids >= 0) & (ids < V)].astype(np.int64)
+            np.bitwise_or.at(hb[b], ids >> 5, np.uint32(1) << (ids & 31).astype(np.uint32))
+        bits_kw = dict(seen_bits=t(hb.view(np.int32)), update_seen=True)
+        pen_kw = dict(penalty=t(inp.penalty))
+    elif inp.seen_indptr is not None:
         pen_kw = dict(seen_indptr=t(inp.seen_indptr), seen_ids=t(inp.seen_ids), penalty=t(inp.penalty))
     out_idx = torch.empty(B, dtype=torch.int64, device=dev)
     out_f = torch.empty(B, V, dtype=torch.float32, device=dev) if inp.need_logits else None
@@ -269,7 +282,7 @@ def main():
     def step():
         kps.sample(logits, top_k, top_p, temp, q_arg, seed=seed_arg, step=7, eps=inp.eps, need_logits=inp.need_logits,
                    out_idx=out_idx,
-                   out_filtered=out_f, workspace=wsp, stream=stream, **pen_kw)
+                   out_filtered=out_f, workspace=wsp, stream=stream, **pen_kw, **bits_kw)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -321,23 +334,26 @@ def main():
         kept = (out_f != float("-inf")).sum(dim=1).to(torch.int64)
     else:
         _, f_tmp = kps.sample(logits, top_k, top_p, temp, q_arg, seed=seed_arg, step=7, eps=inp.eps, need_logits=True,
-                              workspace=wsp, **pen_kw)
+                              workspace=wsp, **pen_kw, **bits_kw)
         kept = (f_tmp != float("-inf")).sum(dim=1).to(torch.int64)
         del f_tmp
-    nnz = int(inp.seen_ids.size) if inp.seen_ids is not None else 0
+    nnz = int(inp.seen_ids.size) if "seen_ids" in pen_kw else 0
+    bits_bytes = B * ((V + 31) // 32) * 4 if bits_kw else 0  # every word of each row's seen bits
     q_kept = int(kept.sum().item()) * 4 if args.draws == "supplied" else 0  # q read at the kept indices
-    alg_bytes = (B * V * esize + (B * V * 4 if inp.need_logits else 0) + q_kept + nnz * 4
-                 + B * (4 * 4 + 8 + (4 if pen_kw else 0)))
+    alg_bytes = (B * V * esize + (B * V * 4 if inp.need_logits else 0) + q_kept + nnz * 4 + bits_bytes
+                 + B * (4 * 4 + 8 + (4 if nnz else 0)))
     metric_bytes = inp.metric_bytes() - (0 if args.draws == "supplied" else B * V * 4)  # no q without supplied draws
     peaks = measured_peaks()
     achieved_gbs = alg_bytes / (kernel_ms / 1e3) / 1e9
-    traffic = ncu_traffic_per_launch(kernel_name, args.workload)
+    # the committed capture is of the default inputs (supplied draws, seen id lists)
+    default_inputs = args.draws == "supplied" and not bits_kw
+    traffic = ncu_traffic_per_launch(kernel_name, args.workload) if default_inputs else None
 
     # ---- end to end through the public API: pinned host inputs in, results out ---------------
     h = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
     h_logits = h(inp.logits if inp.dtype == "f32" else inp.logits.view(np.int16))
     h_q, h_k, h_p, h_t = h(inp.q), h(inp.top_k), h(inp.top_p), h(inp.temperature)
-    h_pen = {k: h(getattr(inp, k)) for k in ("seen_indptr", "seen_ids", "penalty")} if pen_kw else {}
+    h_pen = {k: h(getattr(inp, k)) for k in pen_kw}
     h_idx = torch.empty(B, dtype=torch.int64).pin_memory()
     h_out = torch.empty(B, V, dtype=torch.float32).pin_memory() if inp.need_logits else None
     d_logits, d_q = torch.empty_like(logits), torch.empty_like(q)
@@ -359,7 +375,7 @@ def main():
                 v_.copy_(h_pen[k_], non_blocking=True)
             kps.sample(d_logits, d_k, d_p, d_t, d_q if args.draws == "supplied" else None, seed=seed_arg, step=7,
                        eps=inp.eps, need_logits=inp.need_logits, out_idx=out_idx,
-                       out_filtered=out_f, workspace=wsp, stream=stream, **d_pen)
+                       out_filtered=out_f, workspace=wsp, stream=stream, **d_pen, **bits_kw)
             h_idx.copy_(out_idx, non_blocking=True)
             if h_out is not None:
                 h_out.copy_(out_f, non_blocking=True)
@@ -386,7 +402,8 @@ def main():
         "metric": metric_name(args.workload), "value": rows_per_s, "unit": "rows/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": inp.dtype, "data": "synthetic (seeded, see workloads.py)",
-        "config": dict(workload_config(args.workload), **({} if args.draws == "supplied" else {"draws": args.draws})),
+        "config": dict(workload_config(args.workload), **({} if args.draws == "supplied" else {"draws": args.draws}),
+                       **({"seen": "bits kept on the device, emitted token set each step"} if bits_kw else {})),
         "tokens_per_s": rows_per_s,
         "metric_gbs": metric_bytes / (ms_per_step / 1e3) / 1e9,
         "metric_pct_of_8tbs": 100.0 * metric_bytes / (ms_per_step / 1e3) / 1e9 / NOMINAL_HBM_GBS,

@@ -36,7 +36,7 @@ class StepOpts(ctypes.Structure):
     """kps_step_opts (include/kps.h)."""
     _fields_ = [("q", ctypes.c_void_p), ("generate", ctypes.c_int), ("seed", ctypes.c_uint64),
                 ("step", ctypes.c_uint64), ("finished", ctypes.c_void_p), ("eos_id", ctypes.c_int64),
-                ("unfinished", ctypes.c_void_p)]
+                ("unfinished", ctypes.c_void_p), ("seen_bits", ctypes.c_void_p), ("update_seen", ctypes.c_int)]
 
 
 def load_library() -> ctypes.CDLL:
@@ -160,7 +160,8 @@ def sample(logits: torch.Tensor, top_k: torch.Tensor, top_p: torch.Tensor, tempe
            out_idx: Optional[torch.Tensor] = None, out_filtered: Optional[torch.Tensor] = None,
            workspace: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None,
            seed: Optional[int] = None, step: int = 0, finished: Optional[torch.Tensor] = None,
-           eos_id: int = 0, unfinished: Optional[torch.Tensor] = None):
+           eos_id: int = 0, unfinished: Optional[torch.Tensor] = None, seen_bits: Optional[torch.Tensor] = None,
+           update_seen: bool = False):
     """One fused sampling step on the GPU (asynchronous on `stream`).
 
     q: the race's Exp(1) draws [B, V] fp32, or None to sample off (each row's index is
@@ -169,6 +170,9 @@ def sample(logits: torch.Tensor, top_k: torch.Tensor, top_p: torch.Tensor, tempe
     kps_sample_seeded in include/kps.h defines them).
     finished (uint8 [B], updated in place), eos_id, unfinished (int32 [1]): the
     end-of-sequence epilogue of kps_sample_step.
+    seen_bits (int32 [B, ceil(V/32)], bit v % 32 of word v // 32 = token v seen): the
+    seen set in place of seen_indptr/seen_ids; update_seen sets each row's emitted
+    token in it after the step (kps_sample_step).
     Returns (out_idx int64[B], out_filtered float32[B,V] or None).
     """
     lib = load_library()
@@ -193,6 +197,14 @@ def sample(logits: torch.Tensor, top_k: torch.Tensor, top_p: torch.Tensor, tempe
             raise ValueError("seen_indptr, seen_ids and penalty go together")
         _check(seen_ids, "seen_ids", torch.int32, tuple(seen_ids.shape), dev)
         _check(penalty, "penalty", torch.float32, (B,), dev)
+    if seen_bits is not None:
+        if seen_indptr is not None or seen_ids is not None:
+            raise ValueError("pass seen_bits or seen_indptr/seen_ids, not both")
+        _check(seen_bits, "seen_bits", torch.int32, (B, (V + 31) // 32), dev)
+        if penalty is not None:
+            _check(penalty, "penalty", torch.float32, (B,), dev)
+    elif update_seen:
+        raise ValueError("update_seen needs seen_bits")
     if out_idx is None:
         out_idx = torch.empty(B, dtype=torch.int64, device=dev)
     _check(out_idx, "out_idx", torch.int64, (B,), dev)
@@ -205,13 +217,17 @@ def sample(logits: torch.Tensor, top_k: torch.Tensor, top_p: torch.Tensor, tempe
     if workspace is None:
         workspace = new_workspace(B, V, logits.dtype, dev)
     s = stream if stream is not None else torch.cuda.current_stream(dev)
-    if finished is not None:
-        _check(finished, "finished", torch.uint8, (B,), dev)
-        if unfinished is not None:
-            _check(unfinished, "unfinished", torch.int32, (1,), dev)
+    step_call = finished is not None or seen_bits is not None
+    if step_call:
+        if finished is not None:
+            _check(finished, "finished", torch.uint8, (B,), dev)
+            if unfinished is not None:
+                _check(unfinished, "unfinished", torch.int32, (1,), dev)
+        elif unfinished is not None:
+            raise ValueError("unfinished needs finished")
         opts = StepOpts(_ptr(q) if seed is None else None, 0 if seed is None else 1,
                         0 if seed is None else int(seed) & (2**64 - 1), int(step) & (2**64 - 1), _ptr(finished),
-                        int(eos_id), _ptr(unfinished))
+                        int(eos_id), _ptr(unfinished), _ptr(seen_bits), 1 if update_seen else 0)
         st = lib.kps_sample_step(_ptr(logits), dt, B, V, _ptr(top_k), _ptr(top_p), _ptr(temperature),
                                  _ptr(seen_indptr), _ptr(seen_ids), _ptr(penalty), ctypes.byref(opts), float(eps),
                                  1 if need_logits else 0, _ptr(out_idx), _ptr(out_filtered), _ptr(workspace),
@@ -228,7 +244,7 @@ def sample(logits: torch.Tensor, top_k: torch.Tensor, top_p: torch.Tensor, tempe
                             1 if need_logits else 0, _ptr(out_idx), _ptr(out_filtered), _ptr(workspace),
                             workspace.numel(), ctypes.c_void_p(s.cuda_stream))
     if st != 0:
-        raise KpsError(st, "kps_sample_step" if finished is not None else
+        raise KpsError(st, "kps_sample_step" if step_call else
                        "kps_sample_seeded" if seed is not None else "kps_sample")
     return out_idx, out_filtered
 

@@ -123,7 +123,20 @@ struct Params {
   unsigned char* finished;        // [B] end-of-sequence flags (nullptr: no epilogue)
   long long eos;                  // the end-of-sequence token
   int* unfinished;                // rows still unfinished after the step (nullptr: not counted)
+  uint32_t* seen_bits;            // [B, (V + 31) / 32] seen-token bits in place of the seen ids
+  int update_seen;                // set the bit of each row's emitted token after the step
 };
+
+// Words of one row of the seen-token bits.
+__host__ __device__ __forceinline__ int64_t seen_words(int64_t V) { return (V + 31) / 32; }
+
+// Seen word w of a row's bits with the bits of tokens >= V cleared (0 past the row).
+__device__ __forceinline__ uint32_t seen_word_at(const uint32_t* row_bits, int64_t V, int64_t w) {
+  const int64_t hi = V - 32 * w;  // tokens of this word below V
+  if (hi <= 0) return 0u;
+  const uint32_t x = __ldcg(row_bits + w);
+  return hi >= 32 ? x : (x & ((1u << hi) - 1u));
+}
 
 constexpr int kMaxRowList = 256;  // rows one worker (CTA or cluster) may own in a filtered launch
 
@@ -277,6 +290,13 @@ __device__ __forceinline__ long long eos_epilogue(const Params& P, int64_t row, 
   if (now && !was) P.finished[row] = 1;
   if (!now && P.unfinished) atomicAdd(P.unfinished, 1);
   return out;
+}
+
+// The emitted token of a row joins its seen set (every reader of the row's bits in
+// this launch has read them by now: the token depends on what each of them computed).
+__device__ __forceinline__ void seen_append(const Params& P, int64_t row, long long tok) {
+  if (!P.update_seen || tok < 0 || tok >= P.V) return;
+  atomicOr(P.seen_bits + row * seen_words(P.V) + (tok >> 5), 1u << (tok & 31));
 }
 
 __device__ __forceinline__ float softmax_weight(float x, float M) {
@@ -1050,8 +1070,9 @@ __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P)
     const float p = P.top_p[row];
     const float T = P.temperature[row];
     const bool greedyT = !(T > 0.0f) || isinf(T);
-    const bool pen_on = P.seen_indptr && P.seen_ids && P.penalty && (P.penalty[row] > 0.0f);
+    const bool pen_on = ((P.seen_indptr && P.seen_ids) || P.seen_bits) && P.penalty && (P.penalty[row] > 0.0f);
     const float pen = pen_on ? P.penalty[row] : 1.0f;
+    const bool pen_bits = pen_on && P.seen_bits;
     const bool topk_on = k >= 1 && static_cast<int64_t>(k) <= (V < kTopKMax ? V : kTopKMax);
     const bool p_nan = isnan(p);
     const bool single = greedyT || (!p_nan && p <= 0.0f) || (topk_on && k == 1);
@@ -1060,7 +1081,21 @@ __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P)
     // prefetch up to four seen ids per thread while the chunk is in flight
     int32_t pid[4];
     int32_t b0 = 0, b1 = 0;
-    if (pen_on) {
+    if (pen_bits) {
+      // the chunk's seen bits: bit li of word w is token c0 + 32 w + li (a chunk starts on
+      // a multiple of 8, so a word of it may straddle two words of the row)
+      const uint32_t* rb = P.seen_bits + row * seen_words(V);
+      const int sh = c0 & 31;
+      const int64_t w0 = c0 >> 5;
+      for (int w = threadIdx.x; w < (n + 31) / 32; w += kThreads) {
+        const uint32_t lo = seen_word_at(rb, V, w0 + w);
+        const uint32_t hi = sh ? seen_word_at(rb, V, w0 + w + 1) : 0u;
+        uint32_t x = __funnelshift_r(lo, hi, sh);
+        const int left = n - 32 * w;  // chunk elements in this word
+        if (left < 32) x &= (1u << left) - 1u;
+        bitmap[w] = x;
+      }
+    } else if (pen_on) {
       b0 = P.seen_indptr[row];
       b1 = P.seen_indptr[row + 1];
 #pragma unroll
@@ -1091,7 +1126,16 @@ __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P)
     __syncthreads();
 
     // ---- repetition penalty: scatter over the seen ids, once per distinct id -----------
-    if (pen_on) {
+    if (pen_bits) {
+      for (int w = threadIdx.x; w < (n + 31) / 32; w += kThreads) {
+        for (uint32_t x = bitmap[w]; x; x &= x - 1u) {
+          const int li = 32 * w + __ffs(x) - 1;
+          const float s = xs[li];
+          xs[li] = (s > 0.0f) ? __fdiv_rn(s, pen) : __fmul_rn(s, pen);
+        }
+      }
+      __syncthreads();
+    } else if (pen_on) {
       auto apply = [&](int32_t id) {
         const int32_t li = id - c0;
         if (id >= 0 && static_cast<int64_t>(id) < V && li >= 0 && li < n) {
@@ -1569,7 +1613,11 @@ __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P)
           if (kept_by(c.cand_key[i], c.cand_idx[i], th.key, th.idx)) orow[c.cand_idx[i] - c0] = kfloat(c.cand_key[i]);
       }
     }
-    if (rank == 0 && threadIdx.x == 0) P.out_idx[row] = eos_epilogue(P, row, chosen);
+    if (rank == 0 && threadIdx.x == 0) {
+      const long long tok = eos_epilogue(P, row, chosen);
+      P.out_idx[row] = tok;
+      seen_append(P, row, tok);
+    }
 
     // the chunk buffer is free: start the next row's load if it has not started yet
     __syncthreads();
@@ -1916,7 +1964,7 @@ static kps_status sample_impl(const void* logits, kps_dtype dt, int64_t B, int64
                               int need_logits, int64_t* out_idx, float* out_filtered, void* workspace,
                               size_t workspace_bytes, cudaStream_t stream, int gen, unsigned long long seed,
                               unsigned long long step, unsigned char* finished = nullptr, long long eos = 0,
-                              int* unfinished = nullptr) {
+                              int* unfinished = nullptr, uint32_t* seen_bits = nullptr, int update_seen = 0) {
   if (dt != KPS_F32 && dt != KPS_BF16) return KPS_ERR_INVALID_ARG;
   if (V < 1 || V > INT32_MAX || B < 0) return KPS_ERR_INVALID_ARG;
   if (!(eps >= 0.0f) || std::isinf(eps)) return KPS_ERR_INVALID_ARG;
@@ -1926,7 +1974,10 @@ static kps_status sample_impl(const void* logits, kps_dtype dt, int64_t B, int64
   if (B > INT32_MAX / 16) return KPS_ERR_INVALID_ARG;
   if (!logits || !top_k || !top_p || !temperature || !out_idx) return KPS_ERR_INVALID_ARG;  // q: may be NULL
   if (need_logits && !out_filtered) return KPS_ERR_INVALID_ARG;
-  const bool pen = seen_indptr && seen_ids && penalty;
+  if (seen_bits && (seen_indptr || seen_ids)) return KPS_ERR_INVALID_ARG;  // one form of the seen set
+  if (seen_bits && (reinterpret_cast<uintptr_t>(seen_bits) & 3u) != 0) return KPS_ERR_INVALID_ARG;
+  if (update_seen && !seen_bits) return KPS_ERR_INVALID_ARG;
+  const bool pen = (seen_indptr && seen_ids && penalty) || (seen_bits && penalty);
 
   const size_t esize = dt == KPS_BF16 ? 2 : 4;
   const bool aligned = (reinterpret_cast<uintptr_t>(logits) % 16 == 0) && ((V * esize) % 16 == 0) &&
@@ -1954,9 +2005,11 @@ static kps_status sample_impl(const void* logits, kps_dtype dt, int64_t B, int64
   P.top_k = top_k;
   P.top_p = top_p;
   P.temperature = temperature;
-  P.seen_indptr = pen ? seen_indptr : nullptr;
-  P.seen_ids = pen ? seen_ids : nullptr;
+  P.seen_indptr = pen && !seen_bits ? seen_indptr : nullptr;
+  P.seen_ids = pen && !seen_bits ? seen_ids : nullptr;
   P.penalty = pen ? penalty : nullptr;
+  P.seen_bits = seen_bits;
+  P.update_seen = update_seen ? 1 : 0;
   P.q = gen ? nullptr : q;
   P.gen = gen ? 1 : 0;
   P.seed = seed;
@@ -2083,7 +2136,7 @@ kps_status kps_sample_step(const void* logits, kps_dtype dt, int64_t B, int64_t 
   return sample_impl(logits, dt, B, V, top_k, top_p, temperature, seen_indptr, seen_ids, penalty,
                      opts->generate ? nullptr : opts->q, eps, need_logits, out_idx, out_filtered, workspace,
                      workspace_bytes, stream, opts->generate ? 1 : 0, opts->seed, opts->step, opts->finished,
-                     static_cast<long long>(opts->eos_id), opts->unfinished);
+                     static_cast<long long>(opts->eos_id), opts->unfinished, opts->seen_bits, opts->update_seen);
 }
 
 kps_status kps_set_kernel_policy(int policy) {

@@ -2116,7 +2116,8 @@ __device__ int rbuild_items(const Params& P, int C, int rank, int cluster, int n
 }
 
 // The parameters of a row and its context for part `part` of `nparts` (a team member's
-// share of the vectors); sets the seen bits of the row in the bitmap (which is clear).
+// share of the vectors); sets the seen bits of the row in the bitmap (which is clear), or
+// copies the caller's seen bits of the row into it.
 struct RowFlags {
   int32_t k;
   float p;
@@ -2134,7 +2135,7 @@ __device__ __forceinline__ RowFlags row_setup(const Params& P, int64_t row, cons
   f.p = P.top_p[row];
   const float T = P.temperature[row];
   const bool greedyT = !(T > 0.0f) || isinf(T);
-  f.pen_on = P.seen_indptr && P.seen_ids && P.penalty && (P.penalty[row] > 0.0f);
+  f.pen_on = ((P.seen_indptr && P.seen_ids) || P.seen_bits) && P.penalty && (P.penalty[row] > 0.0f);
   const bool topk_on = f.k >= 1 && static_cast<int64_t>(f.k) <= (P.V < kTopKMax ? P.V : kTopKMax);
   const bool p_nan = isnan(f.p);
   f.single = greedyT || (!p_nan && f.p <= 0.0f) || (topk_on && f.k == 1);
@@ -2165,7 +2166,19 @@ __device__ __forceinline__ RowFlags row_setup(const Params& P, int64_t row, cons
   __syncthreads();  // the bitmap of the previous row is clear
   f.b0 = 0;
   f.b1 = 0;
-  if (f.pen_on) {
+  if (f.pen_on && P.seen_bits) {
+    // the row's seen bits, every word (four loads in flight per thread)
+    const uint32_t* src = P.seen_bits + row * seen_words(P.V);
+    const int W = (V + 31) / 32;
+    for (int w0 = static_cast<int>(threadIdx.x); w0 < W; w0 += 4 * kRT) {
+      uint32_t v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = seen_word_at(src, P.V, w0 + u * kRT);  // 0 past the row
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (w0 + u * kRT < W) sm.bitmap[w0 + u * kRT] = v[u];
+    }
+  } else if (f.pen_on) {
     f.b0 = P.seen_indptr[row];
     f.b1 = P.seen_indptr[row + 1];
     for (int32_t t = f.b0 + static_cast<int32_t>(threadIdx.x); t < f.b1; t += kRT) {
@@ -2177,9 +2190,9 @@ __device__ __forceinline__ RowFlags row_setup(const Params& P, int64_t row, cons
   if (sample) rsample_finish(rc, sl, reinterpret_cast<uint32_t*>(sm.wbuf));
   return f;
 }
-// Clears the row's seen bits again.
+// Clears the row's seen bits again (seen bits given: the next row overwrites every word).
 __device__ __forceinline__ void row_teardown(const Params& P, int64_t row, const RowFlags& f, const RowSmem& sm) {
-  if (!f.pen_on) return;
+  if (!f.pen_on || P.seen_bits) return;
   const int V = static_cast<int>(P.V);
   for (int32_t t = f.b0 + static_cast<int32_t>(threadIdx.x); t < f.b1; t += kRT) {
     const int32_t id = P.seen_ids[t];
@@ -2319,7 +2332,11 @@ __global__ void __launch_bounds__(kRT, 2) kps_row_kernel(const Params P) {
       if (ord >= 0) rec = prec_at(P, ord);
       chosen = rwide_row<kBF16>(rc, sm, tm, f.topp_on, f.p, P.eps, P.exact != 0, ord >= 0 ? &rec : nullptr);
     }
-    if (threadIdx.x == 0 && chosen >= 0) P.out_idx[row] = eos_epilogue(P, row, chosen);
+    if (threadIdx.x == 0 && chosen >= 0) {
+      const long long tok = eos_epilogue(P, row, chosen);
+      P.out_idx[row] = tok;
+      seen_append(P, row, tok);
+    }
     __syncthreads();
     row_teardown(P, row, f, sm);
   }

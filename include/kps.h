@@ -4,7 +4,8 @@
  * One call runs the whole per-step sampling post-process over a [B, V]
  * logits matrix, row by row:
  *
- *   1. repetition penalty over the row's seen ids
+ *   1. repetition penalty over the row's seen ids (a CSR list, or with
+ *        kps_sample_step a bit set kept on the device across steps)
  *        x = x > 0 ? x / penalty : x * penalty, once per distinct id
  *        (MiniMind "Chapter 10: inference generation", §10.7; the C++
  *        post-processing blog, repetition_penalty section);
@@ -143,11 +144,15 @@ kps_status kps_sample_seeded(const void* logits, kps_dtype dt, int64_t B, int64_
 
 /*
  * kps_sample_step — one decode step's sampling with every option: the draws
- * (supplied, generated or none) and the end-of-sequence epilogue of a
+ * (supplied, generated or none), the end-of-sequence epilogue of a
  * generation loop (MiniMind, "Chapter 10: inference generation", the
  * generate loop: a finished sequence emits the end-of-sequence token, a
  * sequence that emits it becomes finished, and the loop stops once all are
- * finished), applied inside the kernel as each row's index is written.
+ * finished), applied inside the kernel as each row's index is written, and
+ * a seen set kept on the device across steps (the same chapter's
+ * repetition penalty runs over the distinct ids of the sequence so far, to
+ * which each step appends its token: with seen_bits and update_seen the
+ * kernel sets that token's bit instead of the caller rebuilding the list).
  */
 typedef struct {
   const float* q;            /* [B, V] fp32 draws as for kps_sample, or NULL
@@ -163,6 +168,20 @@ typedef struct {
   int* unfinished;           /* device int, or NULL: set to the number of rows
                                 left unfinished after the step (0: the loop can
                                 stop).  Requires finished. */
+  uint32_t* seen_bits;       /* [B, (V + 31) / 32] uint32 device, 4-byte aligned,
+                                or NULL: the seen set as bits in place of the
+                                seen ids (bit v % 32 of word b * ((V + 31) / 32)
+                                + v / 32 marks token v of row b; bits of tokens
+                                >= V are ignored).  With seen_bits the
+                                seen_indptr and seen_ids arguments must be NULL
+                                (KPS_ERR_INVALID_ARG otherwise); the penalty runs
+                                when penalty is non-NULL, as with the ids. */
+  int update_seen;           /* non-zero: after the step each row's emitted token
+                                (the index written to out_idx, after the
+                                end-of-sequence epilogue) joins its seen set, the
+                                one bit set in place — the generate loop's
+                                appended token, so the next step needs no new
+                                seen list.  Requires seen_bits. */
 } kps_step_opts;
 
 kps_status kps_sample_step(const void* logits, kps_dtype dt, int64_t B, int64_t V,

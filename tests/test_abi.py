@@ -48,6 +48,11 @@ def test_status_strings(lib):
         assert lib.kps_status_string(code)
 
 
+def _gpu_present() -> bool:
+    import torch
+    return torch.cuda.is_available()
+
+
 def _call(lib, **over):
     fake = ctypes.c_void_p(1 << 20)  # never dereferenced: the host checks run first
     args = dict(logits=fake, dt=0, B=4, V=100, top_k=fake, top_p=fake, temperature=fake, seen_indptr=None,
@@ -69,7 +74,8 @@ def test_host_validation_without_gpu(lib):
     assert _call(lib, workspace_bytes=8) == 3
     assert _call(lib, B=0) == 0  # valid no-op, nothing launched
     assert _call(lib, logits=None) == 1
-    assert _call(lib, q=None) not in (1, 3)  # sampling off: a valid call (here it fails only for want of a GPU)
+    if not _gpu_present():  # a valid call would launch on the fake pointers
+        assert _call(lib, q=None) not in (1, 3)  # sampling off: valid (fails only for want of a GPU)
     assert _call(lib, out_idx=None) == 1
     assert _call(lib, need_logits=1, out_filtered=None) == 1
 
@@ -94,3 +100,33 @@ def test_step_options_are_checked_without_gpu(lib):
     args[10] = ctypes.byref(o)
     assert lib.kps_sample_step(*args) == 1
 
+
+
+def test_seen_bit_options_are_checked_without_gpu(lib):
+    fake = ctypes.c_void_p(1 << 20)
+    lib.kps_sample_step.restype = ctypes.c_int
+    from decode_token_sampling_gb300 import StepOpts
+    args = [fake, 0, 4, 100, fake, fake, fake, None, None, fake, None, ctypes.c_float(1e-20), 0, fake, None,
+            ctypes.c_void_p(1 << 20), ctypes.c_size_t(256), None]
+    # the bit form and the id list together
+    o = StepOpts(None, 0, 0, 0, None, 0, None, fake, 0)
+    args[10] = ctypes.byref(o)
+    args[7], args[8] = fake, fake
+    assert lib.kps_sample_step(*args) == 1
+    args[7], args[8] = None, fake
+    assert lib.kps_sample_step(*args) == 1
+    args[7], args[8] = None, None
+    # a misaligned bit matrix
+    o2 = StepOpts(None, 0, 0, 0, None, 0, None, ctypes.c_void_p((1 << 20) + 2), 0)
+    args[10] = ctypes.byref(o2)
+    assert lib.kps_sample_step(*args) == 1
+    # an update without bits
+    o3 = StepOpts(None, 0, 0, 0, None, 0, None, None, 1)
+    args[10] = ctypes.byref(o3)
+    assert lib.kps_sample_step(*args) == 1
+    # a valid call with bits (and the update) reaches the GPU step: a CUDA error without one
+    # (never run where a GPU would launch on the fake pointers)
+    if not _gpu_present():
+        o4 = StepOpts(None, 0, 0, 0, None, 0, None, fake, 1)
+        args[10] = ctypes.byref(o4)
+        assert lib.kps_sample_step(*args) not in (1, 3)

@@ -322,3 +322,117 @@ def test_eos_epilogue(kernel, draws):
     assert np.array_equal(fin.cpu().numpy(), ref_fin) or near.any()
     assert int(unf.item()) == left or near.any()
     assert (got[fin0 == 1] == eos).all()
+
+
+def _bits_from_ids(inp, rng=None):
+    """The workload's seen lists as a uint32 bit matrix [B, ceil(V/32)] (input side: set the
+    bit of every in-range id; with rng, random bits above V in the last word as well)."""
+    V = inp.V
+    W = (V + 31) // 32
+    bits = np.zeros((inp.B, W), np.uint32)
+    for b in range(inp.B):
+        ids = inp.seen_ids[inp.seen_indptr[b]:inp.seen_indptr[b + 1]]
+        ids = ids[(ids >= 0) & (ids < V)].astype(np.int64)
+        np.bitwise_or.at(bits[b], ids >> 5, (np.uint32(1) << (ids & 31).astype(np.uint32)))
+        if rng is not None and V % 32:
+            bits[b, W - 1] |= np.uint32(int(rng.integers(1, 2**32)) & ~((1 << (V % 32)) - 1) & 0xFFFFFFFF)
+    return bits
+
+
+def _run_bits(inp, bits, update, dev="cuda:0", **extra):
+    import torch
+    import decode_token_sampling_gb300 as kps
+    from parity import to_dev
+    if inp.dtype == "bf16":
+        logits = to_dev(inp.logits.view(np.int16), dev).view(torch.bfloat16)
+    else:
+        logits = to_dev(inp.logits, dev)
+    tb = to_dev(bits.view(np.int32), dev)
+    idx, filt = kps.sample(logits, to_dev(inp.top_k, dev), to_dev(inp.top_p, dev), to_dev(inp.temperature, dev),
+                           to_dev(inp.q, dev) if "seed" not in extra else None, eps=inp.eps,
+                           need_logits=inp.need_logits, penalty=to_dev(inp.penalty, dev), seen_bits=tb,
+                           update_seen=update, **extra)
+    torch.cuda.synchronize()
+    return idx.cpu().numpy(), (filt.cpu().numpy() if filt is not None else None), tb.cpu().numpy().view(np.uint32)
+
+
+@pytest.mark.parametrize("name", ["batch256_penalty", "single_row_long"])
+@pytest.mark.parametrize("update", [False, True])
+def test_seen_bits_match_the_id_lists(name, update, kernel):
+    """The seen set given as bits (with junk above V) gives the oracle's result over the id
+    list; with the update the emitted token's bit, and only it, is set afterwards."""
+    inp = make_workload(name)
+    ref = oracle.sample(inp)
+    bits0 = _bits_from_ids(inp, np.random.default_rng(9))
+    gi, gf, after = _run_bits(inp, bits0.copy(), update)
+    compare(inp, ref, gi, gf, f"{name} bits [{kernel}]")
+    want = bits0.copy()
+    if update:
+        oracle.seen_append(want, gi.astype(np.int64), inp.V)
+    np.testing.assert_array_equal(after, want)
+
+
+@pytest.mark.parametrize("V", [7, 33, 1025, 4099, 40000, 40960])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_seen_bits_ragged_vocab(V, dtype, kernel):
+    """Chunk starts that are not multiples of 32 (the cluster kernel's shifted words) and
+    ragged last words."""
+    inp = make_random(6, V, seed=V + 1, dtype=dtype, penalty=1.3, n_seen=min(3 * V, 200))
+    ref = oracle.sample(inp)
+    bits0 = _bits_from_ids(inp, np.random.default_rng(V))
+    gi, gf, after = _run_bits(inp, bits0.copy(), True)
+    compare(inp, ref, gi, gf, f"V={V} {dtype} bits")
+    want = bits0.copy()
+    oracle.seen_append(want, gi.astype(np.int64), V)
+    np.testing.assert_array_equal(after, want)
+
+
+def test_seen_bits_across_decode_steps(kernel):
+    """Four decode steps on the device: generated draws, the end-of-sequence epilogue and the
+    seen bits updated in place, against the oracle's loop over growing id lists.  Rows at a
+    near-tie (wide top-p rows whose boundary mass gap is below 1e-6 of S) may choose otherwise:
+    there the GPU's token must be one it kept, and both loops carry that token on."""
+    import torch
+    import decode_token_sampling_gb300 as kps
+    from parity import NEAR, to_dev
+    dev = "cuda:0"
+    inp = make_workload("batch256_penalty", rows=range(0, 256, 4))
+    B, V = inp.B, inp.V
+    seqs = [list(inp.seen_ids[inp.seen_indptr[b]:inp.seen_indptr[b + 1]]) for b in range(B)]
+    bits = to_dev(_bits_from_ids(inp).view(np.int32), dev)
+    fin = torch.zeros(B, dtype=torch.uint8, device=dev)
+    fin_ref = np.zeros(B, np.uint8)
+    unf = torch.zeros(1, dtype=torch.int32, device=dev)
+    rng = np.random.default_rng(31)
+    seed = 99
+    eos = None
+    for step in range(4):
+        x = (inp.logits + rng.normal(0, 0.5, inp.logits.shape)).astype(np.float32)
+        indptr = np.cumsum([0] + [len(s) for s in seqs]).astype(np.int32)
+        ids = np.concatenate(seqs).astype(np.int32)
+        q = oracle.exp_draws(B, V, seed, step)
+        ref = oracle.sample_arrays(x, "f32", inp.top_k, inp.top_p, inp.temperature, q, inp.eps, True,
+                                   indptr, ids, inp.penalty)
+        if eos is None:
+            eos = int(ref["idx"][1])  # some row emits eos at the first step
+        idx, filt = kps.sample(to_dev(x, dev), to_dev(inp.top_k, dev), to_dev(inp.top_p, dev),
+                               to_dev(inp.temperature, dev), None, seed=seed, step=step, eps=inp.eps,
+                               need_logits=True, penalty=to_dev(inp.penalty, dev), seen_bits=bits,
+                               update_seen=True, finished=fin, eos_id=eos, unfinished=unf)
+        torch.cuda.synchronize()
+        got = idx.cpu().numpy()
+        gf = filt.cpu().numpy()
+        near = (ref["race_gap"] < NEAR) | (ref["topp_gap"] < NEAR)
+        chosen = ref["idx"].copy()
+        for b in np.nonzero(near & (fin_ref == 0))[0]:
+            assert 0 <= got[b] < V and gf[b, got[b]] != -np.inf, (step, b)
+            chosen[b] = got[b]
+        left = oracle.eos_epilogue(chosen, fin_ref, eos)
+        np.testing.assert_array_equal(got, chosen)
+        np.testing.assert_array_equal(fin.cpu().numpy(), fin_ref)
+        assert int(unf.item()) == left
+        for b in range(B):
+            seqs[b].append(int(chosen[b]))
+    indptr, ids = oracle.seen_ids_from_bits(bits.cpu().numpy().view(np.uint32), V)
+    for b in range(B):
+        assert ids[indptr[b]:indptr[b + 1]].tolist() == sorted(set(int(v) for v in seqs[b] if 0 <= v < V))
