@@ -2115,6 +2115,40 @@ __device__ int rbuild_items(const Params& P, int C, int rank, int cluster, int n
   return static_cast<int>(mine);
 }
 
+// Copies a row's seen bits (V <= kRMaxV tokens; bits of tokens >= V cleared) into the
+// bitmap: 16-byte loads, all in flight at once, when the row's words allow them.
+__device__ __forceinline__ void rseen_copy(const uint32_t* src, int V, uint32_t* bitmap) {
+  const int W = (V + 31) / 32;
+  if ((W & 3) == 0 && (reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
+    constexpr int kPer = (kRMaxV / 128 + kRT - 1) / kRT;  // 16-byte vectors per thread
+    const int W4 = W / 4;
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    uint4 v[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int i = static_cast<int>(threadIdx.x) + u * kRT;
+      v[u] = i < W4 ? __ldcg(s4 + i) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int i = static_cast<int>(threadIdx.x) + u * kRT;
+      if (i < W4) {
+        if (i == W4 - 1 && (V & 31)) v[u].w &= (1u << (V & 31)) - 1u;
+        reinterpret_cast<uint4*>(bitmap)[i] = v[u];
+      }
+    }
+  } else {
+    for (int w0 = static_cast<int>(threadIdx.x); w0 < W; w0 += 4 * kRT) {
+      uint32_t v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = seen_word_at(src, V, w0 + u * kRT);  // 0 past the row
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (w0 + u * kRT < W) bitmap[w0 + u * kRT] = v[u];
+    }
+  }
+}
+
 // The parameters of a row and its context for part `part` of `nparts` (a team member's
 // share of the vectors); sets the seen bits of the row in the bitmap (which is clear), or
 // copies the caller's seen bits of the row into it.
@@ -2163,22 +2197,13 @@ __device__ __forceinline__ RowFlags row_setup(const Params& P, int64_t row, cons
   // seen ids', transformed once the bitmap is built
   SampleLoads sl;
   if (sample) rsample_fetch<kBF16>(rc, &sl);
+  // the caller's seen bits of the row: their loads ride along with the sample's (no thread
+  // reads the bitmap again before the barrier below)
+  if (f.pen_on && P.seen_bits) rseen_copy(P.seen_bits + row * seen_words(P.V), V, sm.bitmap);
   __syncthreads();  // the bitmap of the previous row is clear
   f.b0 = 0;
   f.b1 = 0;
-  if (f.pen_on && P.seen_bits) {
-    // the row's seen bits, every word (four loads in flight per thread)
-    const uint32_t* src = P.seen_bits + row * seen_words(P.V);
-    const int W = (V + 31) / 32;
-    for (int w0 = static_cast<int>(threadIdx.x); w0 < W; w0 += 4 * kRT) {
-      uint32_t v[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) v[u] = seen_word_at(src, P.V, w0 + u * kRT);  // 0 past the row
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (w0 + u * kRT < W) sm.bitmap[w0 + u * kRT] = v[u];
-    }
-  } else if (f.pen_on) {
+  if (f.pen_on && !P.seen_bits) {
     f.b0 = P.seen_indptr[row];
     f.b1 = P.seen_indptr[row + 1];
     for (int32_t t = f.b0 + static_cast<int32_t>(threadIdx.x); t < f.b1; t += kRT) {
