@@ -372,11 +372,12 @@ def test_seen_bits_match_the_id_lists(name, update, kernel):
     np.testing.assert_array_equal(after, want)
 
 
-@pytest.mark.parametrize("V", [7, 33, 1025, 4099, 40000, 40960])
+@pytest.mark.parametrize("V", [7, 33, 1025, 4092, 4099, 8188, 40000, 40960])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_seen_bits_ragged_vocab(V, dtype, kernel):
     """Chunk starts that are not multiples of 32 (the cluster kernel's shifted words) and
-    ragged last words."""
+    ragged last words (4092 and 8188: whole 16-byte groups of words, the last word part
+    tokens and part padding)."""
     inp = make_random(6, V, seed=V + 1, dtype=dtype, penalty=1.3, n_seen=min(3 * V, 200))
     ref = oracle.sample(inp)
     bits0 = _bits_from_ids(inp, np.random.default_rng(V))
@@ -436,3 +437,24 @@ def test_seen_bits_across_decode_steps(kernel):
     indptr, ids = oracle.seen_ids_from_bits(bits.cpu().numpy().view(np.uint32), V)
     for b in range(B):
         assert ids[indptr[b]:indptr[b + 1]].tolist() == sorted(set(int(v) for v in seqs[b] if 0 <= v < V))
+
+
+def test_seen_bits_tracked_without_penalty(kernel):
+    """Seen bits with no penalty array: the step samples as without a penalty and still
+    appends each row's token to the bits."""
+    import torch
+    import decode_token_sampling_gb300 as kps
+    from parity import to_dev
+    inp = make_random(70, 12296, seed=12, penalty=1.5, n_seen=100)
+    ref = oracle.sample_arrays(inp.logits, "f32", inp.top_k, inp.top_p, inp.temperature, inp.q, inp.eps, True)
+    bits0 = _bits_from_ids(inp)
+    tb = to_dev(bits0.view(np.int32), "cuda:0")
+    idx, filt = kps.sample(to_dev(inp.logits, "cuda:0"), to_dev(inp.top_k, "cuda:0"), to_dev(inp.top_p, "cuda:0"),
+                           to_dev(inp.temperature, "cuda:0"), to_dev(inp.q, "cuda:0"), eps=inp.eps, need_logits=True,
+                           seen_bits=tb, update_seen=True)
+    torch.cuda.synchronize()
+    gi = idx.cpu().numpy()
+    compare(inp, ref, gi, filt.cpu().numpy(), "bits without penalty")
+    want = bits0.copy()
+    oracle.seen_append(want, gi.astype(np.int64), inp.V)
+    np.testing.assert_array_equal(tb.cpu().numpy().view(np.uint32), want)
