@@ -134,6 +134,23 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(values, device):
+    """Each value's maximum over the ranks of the process group (the values as they are
+    without one): every rank ends with the same list."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return list(values)
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_rows_per_s(ws: int, rows_per_rank: int, steps: int, slowest_ms: float) -> float:
+    """Whole-job throughput: the rows every rank sampled over the slowest rank's time."""
+    return ws * rows_per_rank * steps / (slowest_ms / 1e3)
+
+
 def run_reference(args, ws, rank):
     """The CPU oracle, timed on the host cores over a bounded sample of the workload's rows."""
     if rank != 0:
@@ -317,12 +334,9 @@ def main():
     total_ms = t_all0.elapsed_time(t_all1)
     per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     kernel_ms = sum(per_launch_ms) / len(per_launch_ms)
-    if ws > 1:
-        tt = torch.tensor([total_ms, kernel_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        total_ms, kernel_ms = tt.tolist()
+    total_ms, kernel_ms = max_over_ranks([total_ms, kernel_ms], dev)
     ms_per_step = total_ms / args.steps
-    rows_per_s = ws * B * args.steps / (total_ms / 1e3)
+    rows_per_s = job_rows_per_s(ws, B, args.steps, total_ms)
 
     status = kps.last_device_status(wsp, stream)
     if status != 0:
@@ -420,11 +434,8 @@ def main():
     e0, e1 = e2e_run(args.e2e_steps)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-    if ws > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = tt.item()
-    e2e_rows = ws * B / (e2e_ms / 1e3)
+    (e2e_ms,) = max_over_ranks([e2e_ms], dev)
+    e2e_rows = job_rows_per_s(ws, B, 1, e2e_ms)
 
     line = {
         "metric": metric_name(args.workload), "value": rows_per_s, "unit": "rows/s", "n_gpus": ws,
