@@ -1920,17 +1920,27 @@ size_t kps_workspace_size(int64_t B, int64_t V, kps_dtype dt) {
 }
 
 int64_t kps_max_vocab(kps_dtype dt) {
+  if (dt != KPS_F32 && dt != KPS_BF16) return 0;
   const int optin = kps::device_smem_optin();
   if (optin <= 0) return 0;
   const bool bf = dt == KPS_BF16;
-  // largest chunk that fits one CTA, times the widest cluster
-  int lo = 8, hi = kps::kMaxChunk;
+  if ((bf ? kps::prepare_kernel<true>() : kps::prepare_kernel<false>()) != cudaSuccess) return 0;
+  // the largest chunk (a multiple of 8) whose layout fits one CTA: binary search over its
+  // eighths, keeping a chunk that fits in lo
+  int lo = 0, hi = kps::kMaxChunk / 8;
   while (lo < hi) {
-    const int mid = ((lo + hi + 1) / 2) / 8 * 8;
-    if (mid <= lo) break;
-    if (kps::make_layout(mid, bf).total <= static_cast<size_t>(optin)) lo = mid; else hi = mid - 8;
+    const int mid = (lo + hi + 1) / 2;
+    if (kps::make_layout(mid * 8, bf).total <= static_cast<size_t>(optin)) lo = mid; else hi = mid - 1;
   }
-  return static_cast<int64_t>(lo) * 16;
+  if (lo == 0) return 0;
+  const int nc = lo * 8;
+  const size_t smem = kps::make_layout(nc, bf).total;
+  // times the widest cluster the device runs with that much shared memory per CTA
+  for (int cs = 16; cs >= 1; cs /= 2) {
+    const bool fits = bf ? kps::cluster_fits<true>(cs, smem) : kps::cluster_fits<false>(cs, smem);
+    if (fits) return static_cast<int64_t>(nc) * cs;
+  }
+  return 0;
 }
 
 const char* kps_status_string(kps_status s) {

@@ -458,3 +458,52 @@ def test_seen_bits_tracked_without_penalty(kernel):
     want = bits0.copy()
     oracle.seen_append(want, gi.astype(np.int64), inp.V)
     np.testing.assert_array_equal(tb.cpu().numpy().view(np.uint32), want)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_largest_vocabulary_and_one_past_it(dtype):
+    """At the largest vocabulary the library takes (one row spread over the widest cluster)
+    the rows match the oracle; a vocabulary past it is refused on the host, before any launch."""
+    import torch
+    import decode_token_sampling_gb300 as kps
+    code = 1 if dtype == "bf16" else 0
+    vmax = int(kps.load_library().kps_max_vocab(code))
+    assert vmax >= 262144
+    inp = make_random(2, vmax, seed=77, dtype=dtype, penalty=1.2, n_seen=300)
+    ref = oracle.sample(inp)
+    gi, gf = run_gpu(inp)
+    compare(inp, ref, gi, gf, f"V={vmax} {dtype}")
+    big = make_random(2, vmax + 8, seed=78, dtype=dtype)
+    with pytest.raises(kps.KpsError) as e:
+        run_gpu(big)
+    assert e.value.code == 2  # KPS_ERR_UNSUPPORTED
+
+
+def test_row_kernel_at_its_largest_vocabulary():
+    """V = 262144 fp32 over 64 rows: the row kernel's largest row (its seen bitmap fills the
+    shared-memory slot it has)."""
+    import decode_token_sampling_gb300 as kps
+    kps.set_kernel_policy(kps.KERNEL_ROW)
+    try:
+        inp = make_random(64, 262144, seed=79, penalty=1.2, n_seen=300, need_logits=True)
+        ref = oracle.sample(inp)
+        gi, gf = run_gpu(inp)
+        assert kps.last_kernel() == "kps_row_kernel"
+        compare(inp, ref, gi, gf, "row kernel V=262144")
+    finally:
+        kps.set_kernel_policy(kps.KERNEL_AUTO)
+
+
+def test_more_work_units_than_the_item_list_holds():
+    """80000 rows of 16 tokens: more units per cluster than the row kernel's item list holds,
+    so every CTA takes rows on its own, round-robin."""
+    import decode_token_sampling_gb300 as kps
+    kps.set_kernel_policy(kps.KERNEL_ROW)
+    try:
+        inp = make_random(80000, 16, seed=80, penalty=1.2, n_seen=8, need_logits=True)
+        ref = oracle.sample(inp)
+        gi, gf = run_gpu(inp)
+        assert kps.last_kernel() == "kps_row_kernel"
+        compare(inp, ref, gi, gf, "B=80000 V=16")
+    finally:
+        kps.set_kernel_policy(kps.KERNEL_AUTO)
