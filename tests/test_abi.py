@@ -130,3 +130,25 @@ def test_seen_bit_options_are_checked_without_gpu(lib):
         o4 = StepOpts(None, 0, 0, 0, None, 0, None, fake, 1)
         args[10] = ctypes.byref(o4)
         assert lib.kps_sample_step(*args) not in (1, 3)
+
+
+def test_step_opts_layout_matches_the_header(tmp_path):
+    """The binding's kps_step_opts has the header's field offsets and size (checked by
+    compiling a C program against include/kps.h)."""
+    import shutil
+    import subprocess
+    from decode_token_sampling_gb300 import StepOpts
+    cc = shutil.which("gcc") or shutil.which("cc")
+    cuda_inc = "/usr/local/cuda/include"
+    if cc is None or not os.path.exists(os.path.join(cuda_inc, "cuda_runtime_api.h")):
+        pytest.skip("no C compiler or CUDA headers")
+    fields = [name for name, _ in StepOpts._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "kps.h"\nint main(void) {\n'
+                   + "".join(f'  printf("%zu\\n", offsetof(kps_step_opts, {f}));\n' for f in fields)
+                   + '  printf("%zu\\n", sizeof(kps_step_opts));\n  return 0;\n}\n')
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", os.path.join(ROOT, "include"), "-I", cuda_inc, "-o", str(exe), str(src)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    want = [getattr(StepOpts, f).offset for f in fields] + [ctypes.sizeof(StepOpts)]
+    assert got == want
