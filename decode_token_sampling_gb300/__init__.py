@@ -11,6 +11,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import threading
 from typing import Optional, Tuple
 
 import torch
@@ -36,7 +37,8 @@ class StepOpts(ctypes.Structure):
     """kps_step_opts (include/kps.h)."""
     _fields_ = [("q", ctypes.c_void_p), ("generate", ctypes.c_int), ("seed", ctypes.c_uint64),
                 ("step", ctypes.c_uint64), ("finished", ctypes.c_void_p), ("eos_id", ctypes.c_int64),
-                ("unfinished", ctypes.c_void_p), ("seen_bits", ctypes.c_void_p), ("update_seen", ctypes.c_int)]
+                ("unfinished", ctypes.c_void_p), ("seen_bits", ctypes.c_void_p), ("update_seen", ctypes.c_int),
+                ("kernel_policy", ctypes.c_int)]
 
 
 def load_library() -> ctypes.CDLL:
@@ -64,14 +66,12 @@ def load_library() -> ctypes.CDLL:
     lib.kps_sample_step.restype = I32
     lib.kps_sample_step.argtypes = [P, I32, I64, I64, P, P, P, P, P, P, ctypes.POINTER(StepOpts), ctypes.c_float,
                                     I32, P, P, P, ctypes.c_size_t, P]
-    lib.kps_set_kernel_policy.restype = I32
-    lib.kps_set_kernel_policy.argtypes = [I32]
-    lib.kps_get_kernel_policy.restype = I32
-    lib.kps_get_kernel_policy.argtypes = []
     lib.kps_last_kernel.restype = I32
     lib.kps_last_kernel.argtypes = []
     lib.kps_last_launch_count.restype = I32
     lib.kps_last_launch_count.argtypes = []
+    lib.kps_last_cluster_size.restype = I32
+    lib.kps_last_cluster_size.argtypes = []
     lib.kps_query_launch.restype = I32
     lib.kps_query_launch.argtypes = [I64, I64, I32, ctypes.POINTER(I32), ctypes.POINTER(I64),
                                      ctypes.POINTER(ctypes.c_size_t)]
@@ -119,16 +119,20 @@ def new_workspace(B: int, V: int, dtype: torch.dtype = torch.float32, device="cu
 
 KERNEL_AUTO, KERNEL_CLUSTER, KERNEL_ROW, KERNEL_ROW_EXACT = 0, 1, 2, 3
 
+_local = threading.local()
+
 
 def set_kernel_policy(policy: int) -> None:
-    """Process-wide kernel choice: KERNEL_AUTO, KERNEL_CLUSTER, KERNEL_ROW or KERNEL_ROW_EXACT (see include/kps.h)."""
-    st = load_library().kps_set_kernel_policy(int(policy))
-    if st != 0:
-        raise KpsError(st, "kps_set_kernel_policy")
+    """This thread's default kernel choice for sample() calls that pass no `kernel`:
+    KERNEL_AUTO, KERNEL_CLUSTER, KERNEL_ROW or KERNEL_ROW_EXACT (kps_step_opts.kernel_policy in
+    include/kps.h).  The library itself keeps no choice: it goes with each call."""
+    if policy not in (KERNEL_AUTO, KERNEL_CLUSTER, KERNEL_ROW, KERNEL_ROW_EXACT):
+        raise ValueError(f"unknown kernel policy {policy}")
+    _local.policy = int(policy)
 
 
 def get_kernel_policy() -> int:
-    return int(load_library().kps_get_kernel_policy())
+    return getattr(_local, "policy", KERNEL_AUTO)
 
 
 KERNEL_NAMES = {1: "kps_sample_kernel", 2: "kps_row_kernel"}
@@ -142,6 +146,11 @@ def last_kernel() -> str:
 def last_launch_count() -> int:
     """Kernels this thread's most recent launching sample() call queued (2: pre-pass + row kernel)."""
     return int(load_library().kps_last_launch_count())
+
+
+def last_cluster_size() -> int:
+    """CTAs per cluster of the kernel this thread's most recent launching sample() call used."""
+    return int(load_library().kps_last_cluster_size())
 
 
 def query_launch(B: int, V: int, dtype: torch.dtype = torch.float32) -> dict:
@@ -161,7 +170,7 @@ def sample(logits: torch.Tensor, top_k: torch.Tensor, top_p: torch.Tensor, tempe
            workspace: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None,
            seed: Optional[int] = None, step: int = 0, finished: Optional[torch.Tensor] = None,
            eos_id: int = 0, unfinished: Optional[torch.Tensor] = None, seen_bits: Optional[torch.Tensor] = None,
-           update_seen: bool = False):
+           update_seen: bool = False, kernel: Optional[int] = None):
     """One fused sampling step on the GPU (asynchronous on `stream`).
 
     q: the race's Exp(1) draws [B, V] fp32, or None to sample off (each row's index is
@@ -173,6 +182,8 @@ def sample(logits: torch.Tensor, top_k: torch.Tensor, top_p: torch.Tensor, tempe
     seen_bits (int32 [B, ceil(V/32)], bit v % 32 of word v // 32 = token v seen): the
     seen set in place of seen_indptr/seen_ids; update_seen sets each row's emitted
     token in it after the step (kps_sample_step).
+    kernel: the kernel policy of this call (KERNEL_*; default: this thread's
+    set_kernel_policy choice, else automatic).
     Returns (out_idx int64[B], out_filtered float32[B,V] or None).
     """
     lib = load_library()
@@ -217,7 +228,8 @@ def sample(logits: torch.Tensor, top_k: torch.Tensor, top_p: torch.Tensor, tempe
     if workspace is None:
         workspace = new_workspace(B, V, logits.dtype, dev)
     s = stream if stream is not None else torch.cuda.current_stream(dev)
-    step_call = finished is not None or seen_bits is not None
+    policy = get_kernel_policy() if kernel is None else int(kernel)
+    step_call = finished is not None or seen_bits is not None or policy != KERNEL_AUTO
     if step_call:
         if finished is not None:
             _check(finished, "finished", torch.uint8, (B,), dev)
@@ -227,7 +239,7 @@ def sample(logits: torch.Tensor, top_k: torch.Tensor, top_p: torch.Tensor, tempe
             raise ValueError("unfinished needs finished")
         opts = StepOpts(_ptr(q) if seed is None else None, 0 if seed is None else 1,
                         0 if seed is None else int(seed) & (2**64 - 1), int(step) & (2**64 - 1), _ptr(finished),
-                        int(eos_id), _ptr(unfinished), _ptr(seen_bits), 1 if update_seen else 0)
+                        int(eos_id), _ptr(unfinished), _ptr(seen_bits), 1 if update_seen else 0, policy)
         st = lib.kps_sample_step(_ptr(logits), dt, B, V, _ptr(top_k), _ptr(top_p), _ptr(temperature),
                                  _ptr(seen_indptr), _ptr(seen_ids), _ptr(penalty), ctypes.byref(opts), float(eps),
                                  1 if need_logits else 0, _ptr(out_idx), _ptr(out_filtered), _ptr(workspace),

@@ -55,6 +55,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cooperative_groups.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <climits>
 #include <cmath>
@@ -1723,51 +1724,78 @@ static bool cluster_fits(int cs, size_t smem) {
   return n > 0;
 }
 
-// Chooses the cluster size: the smallest power of two whose per-CTA chunk fits
-// two CTAs per SM, else the smallest that fits at all; then, for small
-// batches, wider clusters so more SMs work on each row.
+// The cluster kernel's shapes for one (device, dtype, V), independent of the batch: for each
+// power-of-two cluster size whether it runs, its chunk, shared memory and resident clusters,
+// and the base size (the smallest whose per-CTA chunk fits two CTAs per SM, else the smallest
+// that fits at all).  Occupancy queries are slow, so this is computed once per shape.
+struct ClusterShapes {
+  kps_status status;  // KPS_OK when some size runs
+  int base;           // index into sizes of the base cluster size
+  int sms;
+  int fits[5];
+  int nc[5];
+  size_t smem[5];
+  int clusters[5];
+};
+constexpr int kClusterSizes[5] = {1, 2, 4, 8, 16};
+
+template <bool kBF16>
+static ClusterShapes cluster_shapes(int64_t V) {
+  ClusterShapes cs{};
+  cs.status = KPS_ERR_UNSUPPORTED;
+  cs.base = -1;
+  const int optin = device_smem_optin();
+  cs.sms = device_sm_count();
+  if (optin <= 0 || cs.sms <= 0 || prepare_kernel<kBF16>() != cudaSuccess) {
+    cs.status = KPS_ERR_CUDA;
+    return cs;
+  }
+  for (int i = 0; i < 5; ++i) {
+    const int c = kClusterSizes[i];
+    cs.nc[i] = round_up8((V + c - 1) / c);
+    cs.smem[i] = make_layout(cs.nc[i], kBF16).total;
+    cs.fits[i] = cs.nc[i] <= kMaxChunk && cs.smem[i] <= static_cast<size_t>(optin) && cluster_fits<kBF16>(c, cs.smem[i]);
+    cs.clusters[i] = cs.fits[i] ? active_clusters<kBF16>(c, cs.smem[i]) : 0;
+    if (cs.clusters[i] <= 0) cs.fits[i] = 0;
+  }
+  for (int i = 0; i < 4 && cs.base < 0; ++i)  // sizes up to 8 whose chunk fits two CTAs per SM
+    if (cs.fits[i] && cs.smem[i] <= static_cast<size_t>(kSmemCap2PerSM)) cs.base = i;
+  for (int i = 0; i < 5 && cs.base < 0; ++i)
+    if (cs.fits[i]) cs.base = i;
+  if (cs.base >= 0) cs.status = KPS_OK;
+  return cs;
+}
+
+// The cluster size for a batch of B rows: the base size, widened for small batches so more
+// SMs work on each row (chunks of at least 4096 elements).  Depends on B only through the
+// widening, which every caller computes from the same table.
+static kps_status launch_from_shapes(const ClusterShapes& cs, int64_t B, int64_t V, LaunchCfg* out) {
+  if (cs.status != KPS_OK) return cs.status;
+  int i = cs.base;
+  while (i < 4 && B * kClusterSizes[i] * 2 <= cs.sms && (V + kClusterSizes[i] * 2 - 1) / (kClusterSizes[i] * 2) >= 4096 &&
+         cs.fits[i + 1])
+    ++i;
+  out->cs = kClusterSizes[i];
+  out->nc = cs.nc[i];
+  out->smem = cs.smem[i];
+  out->clusters = cs.clusters[i];
+  return KPS_OK;
+}
+
 template <bool kBF16>
 static kps_status choose_launch(int64_t B, int64_t V, LaunchCfg* out) {
-  const int optin = device_smem_optin();
-  const int sms = device_sm_count();
-  if (optin <= 0 || sms <= 0) return KPS_ERR_CUDA;
-  if (prepare_kernel<kBF16>() != cudaSuccess) return KPS_ERR_CUDA;
-  const int sizes[] = {1, 2, 4, 8, 16};
-  int pick = -1;
-  for (int cs : sizes) {
-    if (cs > 8) break;
-    const int nc = round_up8((V + cs - 1) / cs);
-    if (nc <= kMaxChunk && make_layout(nc, kBF16).total <= static_cast<size_t>(kSmemCap2PerSM)) { pick = cs; break; }
-  }
-  if (pick < 0) {
-    for (int cs : sizes) {
-      const int nc = round_up8((V + cs - 1) / cs);
-      if (nc <= kMaxChunk && make_layout(nc, kBF16).total <= static_cast<size_t>(optin) &&
-          cluster_fits<kBF16>(cs, make_layout(nc, kBF16).total)) { pick = cs; break; }
-    }
-  }
-  if (pick < 0) return KPS_ERR_UNSUPPORTED;
-  // small batches: spread each row over more SMs (chunks of at least 4096 elements)
-  while (pick < 16 && B * pick * 2 <= sms && (V + pick * 2 - 1) / (pick * 2) >= 4096) {
-    const int nc2 = round_up8((V + pick * 2 - 1) / (pick * 2));
-    if (!cluster_fits<kBF16>(pick * 2, make_layout(nc2, kBF16).total)) break;
-    pick *= 2;
-  }
-  out->cs = pick;
-  out->nc = round_up8((V + pick - 1) / pick);
-  out->smem = make_layout(out->nc, kBF16).total;
-  out->clusters = active_clusters<kBF16>(out->cs, out->smem);
-  if (out->clusters <= 0) return KPS_ERR_UNSUPPORTED;
-  return KPS_OK;
+  const ClusterShapes cs = cluster_shapes<kBF16>(V);
+  return launch_from_shapes(cs, B, V, out);
 }
 
 // The kernel the calling thread's last successful kps_sample launched (1 cluster, 2 row).
 static thread_local int t_last_kernel = 0;
 static thread_local int t_last_launches = 0;
+static thread_local int t_last_cluster = 0;  // CTAs per cluster of that launch
 
-// Kernel choice: 0 = automatic, 1 = cluster kernel only, 2 = row kernel where supported,
-// 3 = row kernel with the exact whole-row selection forced (a test hook).
-static int g_policy = 0;
+// Kernel choice, per call (kps_step_opts.kernel_policy): 0 = automatic, 1 = cluster kernel
+// only, 2 = row kernel where supported, 3 = row kernel with the exact whole-row selection
+// forced (a test hook).
 constexpr int64_t kRowMinRows = 64;  // automatic: the row kernel from this batch size up
 constexpr size_t kWorkspaceMin = 256;  // the status word (and its alignment)
 constexpr int64_t kMaxPreRows = 1024;  // top-p-only rows with a pre-pass record, at most
@@ -1848,21 +1876,19 @@ static bool choose_row(int64_t V, RowCfg* out) {
   return false;
 }
 
-// Launch decisions depend only on (device, dtype, V) plus min() with B, so they are
-// computed once and cached: kps_sample then costs one lookup and one launch.
+// Launch decisions depend on (device, dtype, V), plus the batch size only through the
+// cluster kernel's widening (launch_from_shapes, cheap), so the batch-independent part is
+// computed once per shape and cached: kps_sample then costs one lookup and one launch.
 struct CachedShape {
   int dev;
   int dt;
   int64_t V;
   bool row_ok;
   RowCfg row;
-  bool cluster_ok;
-  kps_status cluster_status;
-  LaunchCfg cluster;      // clusters = resident clusters (min with B at launch)
-  bool cluster_small_b;   // cluster choice was made for a batch smaller than the SM count
+  ClusterShapes cluster;
 };
 
-static kps_status lookup_shape(kps_dtype dt, int64_t V, int64_t B, CachedShape* out) {
+static kps_status lookup_shape(kps_dtype dt, int64_t V, CachedShape* out) {
   static std::mutex mu;
   static CachedShape cache[32];
   static int used = 0, next = 0;
@@ -1871,12 +1897,10 @@ static kps_status lookup_shape(kps_dtype dt, int64_t V, int64_t B, CachedShape* 
     (void)cudaGetLastError();
     return KPS_ERR_CUDA;
   }
-  // the cluster size depends on whether the batch fills the SMs (small batches widen clusters)
-  const bool small_b = B * 2 <= device_sm_count();
   std::lock_guard<std::mutex> lock(mu);
   for (int i = 0; i < used; ++i) {
     const CachedShape& c = cache[i];
-    if (c.dev == dev && c.dt == static_cast<int>(dt) && c.V == V && c.cluster_small_b == small_b) {
+    if (c.dev == dev && c.dt == static_cast<int>(dt) && c.V == V) {
       *out = c;
       return KPS_OK;
     }
@@ -1885,16 +1909,10 @@ static kps_status lookup_shape(kps_dtype dt, int64_t V, int64_t B, CachedShape* 
   c.dev = dev;
   c.dt = static_cast<int>(dt);
   c.V = V;
-  c.cluster_small_b = small_b;
-  const int64_t bigB = 1 << 20;
   RowCfg rcfg{};
   c.row_ok = dt == KPS_BF16 ? choose_row<true>(V, &rcfg) : choose_row<false>(V, &rcfg);
   c.row = rcfg;
-  LaunchCfg lc{};
-  const int64_t probeB = small_b ? B : bigB;
-  c.cluster_status = dt == KPS_BF16 ? choose_launch<true>(probeB, V, &lc) : choose_launch<false>(probeB, V, &lc);
-  c.cluster_ok = c.cluster_status == KPS_OK;
-  c.cluster = lc;
+  c.cluster = dt == KPS_BF16 ? cluster_shapes<true>(V) : cluster_shapes<false>(V);
   if (used < 32) {
     cache[used++] = c;
   } else {
@@ -1905,6 +1923,17 @@ static kps_status lookup_shape(kps_dtype dt, int64_t V, int64_t B, CachedShape* 
   return KPS_OK;
 }
 
+}  // namespace kps
+
+namespace kps {
+// An NVTX range around each public sampling call: it names the call in a profiler's timeline
+// (Nsight Systems, ncu's NVTX filters) and costs a pointer check when no tool is attached.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 }  // namespace kps
 
 // ------------------------------------------------------------------------------------------
@@ -1967,6 +1996,21 @@ kps_status kps_query_launch(int64_t B, int64_t V, kps_dtype dt, int* cluster_siz
   return KPS_OK;
 }
 
+// The host-side checks of the arguments every entry point shares (the workspace aside);
+// KPS_OK when the call may go ahead.
+static kps_status check_args(kps_dtype dt, int64_t B, int64_t V, float eps, const void* logits, const int32_t* top_k,
+                             const float* top_p, const float* temperature, const int64_t* out_idx, int need_logits,
+                             const float* out_filtered) {
+  if (dt != KPS_F32 && dt != KPS_BF16) return KPS_ERR_INVALID_ARG;
+  if (V < 1 || V > INT32_MAX || B < 0) return KPS_ERR_INVALID_ARG;
+  if (!(eps >= 0.0f) || std::isinf(eps)) return KPS_ERR_INVALID_ARG;
+  if (B == 0) return KPS_OK;
+  if (B > INT32_MAX / 16) return KPS_ERR_INVALID_ARG;
+  if (!logits || !top_k || !top_p || !temperature || !out_idx) return KPS_ERR_INVALID_ARG;  // q: may be NULL
+  if (need_logits && !out_filtered) return KPS_ERR_INVALID_ARG;
+  return KPS_OK;
+}
+
 // The sampling step; q given (or NULL) or, with gen, generated from (seed, step).
 static kps_status sample_impl(const void* logits, kps_dtype dt, int64_t B, int64_t V, const int32_t* top_k,
                               const float* top_p, const float* temperature, const int32_t* seen_indptr,
@@ -1974,16 +2018,17 @@ static kps_status sample_impl(const void* logits, kps_dtype dt, int64_t B, int64
                               int need_logits, int64_t* out_idx, float* out_filtered, void* workspace,
                               size_t workspace_bytes, cudaStream_t stream, int gen, unsigned long long seed,
                               unsigned long long step, unsigned char* finished = nullptr, long long eos = 0,
-                              int* unfinished = nullptr, uint32_t* seen_bits = nullptr, int update_seen = 0) {
+                              int* unfinished = nullptr, uint32_t* seen_bits = nullptr, int update_seen = 0,
+                              int policy = 0) {
   if (dt != KPS_F32 && dt != KPS_BF16) return KPS_ERR_INVALID_ARG;
   if (V < 1 || V > INT32_MAX || B < 0) return KPS_ERR_INVALID_ARG;
   if (!(eps >= 0.0f) || std::isinf(eps)) return KPS_ERR_INVALID_ARG;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < kps::kWorkspaceMin)
     return KPS_ERR_WORKSPACE;
-  if (B == 0) return KPS_OK;
-  if (B > INT32_MAX / 16) return KPS_ERR_INVALID_ARG;
-  if (!logits || !top_k || !top_p || !temperature || !out_idx) return KPS_ERR_INVALID_ARG;  // q: may be NULL
-  if (need_logits && !out_filtered) return KPS_ERR_INVALID_ARG;
+  {
+    const kps_status st = check_args(dt, B, V, eps, logits, top_k, top_p, temperature, out_idx, need_logits, out_filtered);
+    if (st != KPS_OK || B == 0) return st;
+  }
   if (seen_bits && (seen_indptr || seen_ids)) return KPS_ERR_INVALID_ARG;  // one form of the seen set
   if (seen_bits && (reinterpret_cast<uintptr_t>(seen_bits) & 3u) != 0) return KPS_ERR_INVALID_ARG;
   if (update_seen && !seen_bits) return KPS_ERR_INVALID_ARG;
@@ -1994,18 +2039,18 @@ static kps_status sample_impl(const void* logits, kps_dtype dt, int64_t B, int64
                        (reinterpret_cast<uintptr_t>(q) % 16 == 0) && (V % 4 == 0) &&  // a NULL q is aligned
                        (!need_logits || reinterpret_cast<uintptr_t>(out_filtered) % 16 == 0);
   const bool want_row =
-      aligned && (kps::g_policy >= 2 || (kps::g_policy == 0 && B >= kps::kRowMinRows));
+      aligned && (policy >= 2 || (policy == 0 && B >= kps::kRowMinRows));
   kps::RowCfg rcfg;
-  kps::LaunchCfg cfg;
+  kps::LaunchCfg cfg{};
   bool use_row = false;
   {
     kps::CachedShape cs;
-    const kps_status st = kps::lookup_shape(dt, V, B, &cs);
+    const kps_status st = kps::lookup_shape(dt, V, &cs);
     if (st != KPS_OK) return st;
     use_row = want_row && cs.row_ok;
     rcfg = cs.row;
-    cfg = cs.cluster;
-    if (!use_row && !cs.cluster_ok) return cs.cluster_status;
+    const kps_status cst = kps::launch_from_shapes(cs.cluster, B, V, &cfg);
+    if (!use_row && cst != KPS_OK) return cst;
   }
 
   kps::Params P;
@@ -2039,7 +2084,7 @@ static kps_status sample_impl(const void* logits, kps_dtype dt, int64_t B, int64
   P.nc = cfg.nc;
   P.use_tma = aligned ? 1 : 0;
   P.filter = 0;
-  P.exact = kps::g_policy == 3 ? 1 : 0;
+  P.exact = policy == 3 ? 1 : 0;
   P.pre = nullptr;
   P.pre_rows = 0;
 
@@ -2091,6 +2136,7 @@ static kps_status sample_impl(const void* logits, kps_dtype dt, int64_t B, int64
     }
     kps::t_last_kernel = 2;
     kps::t_last_launches = P.pre ? 2 : 1;
+    kps::t_last_cluster = rcfg.cs;
     return KPS_OK;
   }
 
@@ -2115,6 +2161,7 @@ static kps_status sample_impl(const void* logits, kps_dtype dt, int64_t B, int64
   }
   kps::t_last_kernel = 1;
   kps::t_last_launches = 1;
+  kps::t_last_cluster = cfg.cs;
   return KPS_OK;
 }
 
@@ -2123,6 +2170,7 @@ kps_status kps_sample(const void* logits, kps_dtype dt, int64_t B, int64_t V, co
                       const int32_t* seen_ids, const float* penalty, const float* q, float eps, int need_logits,
                       int64_t* out_idx, float* out_filtered, void* workspace, size_t workspace_bytes,
                       cudaStream_t stream) {
+  const kps::NvtxRange range("kps_sample");
   return sample_impl(logits, dt, B, V, top_k, top_p, temperature, seen_indptr, seen_ids, penalty, q, eps,
                      need_logits, out_idx, out_filtered, workspace, workspace_bytes, stream, 0, 0ull, 0ull);
 }
@@ -2132,6 +2180,7 @@ kps_status kps_sample_seeded(const void* logits, kps_dtype dt, int64_t B, int64_
                              const int32_t* seen_ids, const float* penalty, unsigned long long seed,
                              unsigned long long step, float eps, int need_logits, int64_t* out_idx,
                              float* out_filtered, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  const kps::NvtxRange range("kps_sample_seeded");
   return sample_impl(logits, dt, B, V, top_k, top_p, temperature, seen_indptr, seen_ids, penalty, nullptr, eps,
                      need_logits, out_idx, out_filtered, workspace, workspace_bytes, stream, 1, seed, step);
 }
@@ -2141,25 +2190,22 @@ kps_status kps_sample_step(const void* logits, kps_dtype dt, int64_t B, int64_t 
                            const int32_t* seen_ids, const float* penalty, const kps_step_opts* opts, float eps,
                            int need_logits, int64_t* out_idx, float* out_filtered, void* workspace,
                            size_t workspace_bytes, cudaStream_t stream) {
+  const kps::NvtxRange range("kps_sample_step");
   if (!opts) return KPS_ERR_INVALID_ARG;
   if (opts->unfinished && !opts->finished) return KPS_ERR_INVALID_ARG;
+  if (opts->kernel_policy < 0 || opts->kernel_policy > 3) return KPS_ERR_INVALID_ARG;
   return sample_impl(logits, dt, B, V, top_k, top_p, temperature, seen_indptr, seen_ids, penalty,
                      opts->generate ? nullptr : opts->q, eps, need_logits, out_idx, out_filtered, workspace,
                      workspace_bytes, stream, opts->generate ? 1 : 0, opts->seed, opts->step, opts->finished,
-                     static_cast<long long>(opts->eos_id), opts->unfinished, opts->seen_bits, opts->update_seen);
+                     static_cast<long long>(opts->eos_id), opts->unfinished, opts->seen_bits, opts->update_seen,
+                     opts->kernel_policy);
 }
-
-kps_status kps_set_kernel_policy(int policy) {
-  if (policy < 0 || policy > 3) return KPS_ERR_INVALID_ARG;
-  kps::g_policy = policy;
-  return KPS_OK;
-}
-
-int kps_get_kernel_policy(void) { return kps::g_policy; }
 
 int kps_last_kernel(void) { return kps::t_last_kernel; }
 
 int kps_last_launch_count(void) { return kps::t_last_launches; }
+
+int kps_last_cluster_size(void) { return kps::t_last_cluster; }
 
 kps_status kps_last_device_status(void* workspace, cudaStream_t stream, int* out) {
   if (!workspace || !out) return KPS_ERR_INVALID_ARG;
@@ -2209,9 +2255,13 @@ extern "C" kps_status kps_sample_noalloc(const void* logits, kps_dtype dt, int64
                                          const int32_t* seen_indptr, const int32_t* seen_ids,
                                          const float* penalty, const float* q, float eps, int need_logits,
                                          int64_t* out_idx, float* out_filtered, cudaStream_t stream) {
-  if (kps_workspace_size(B, V, dt) == 0) return KPS_ERR_INVALID_ARG;
+  const kps::NvtxRange range("kps_sample_noalloc");
+  // every argument is checked before the shared array is touched: a rejected call queues nothing
+  {
+    const kps_status st = check_args(dt, B, V, eps, logits, top_k, top_p, temperature, out_idx, need_logits, out_filtered);
+    if (st != KPS_OK || B == 0) return st;
+  }
   const size_t need = kps::kWorkspaceMin;  // the status word; no room for pre-pass records
-  if (B == 0) return KPS_OK;
   void* scratch = kps::noalloc_scratch_address();
   if (!scratch) return KPS_ERR_CUDA;
   // the shared array keeps the previous call's status word: clear it on this stream first

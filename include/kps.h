@@ -182,6 +182,24 @@ typedef struct {
                                 one bit set in place — the generate loop's
                                 appended token, so the next step needs no new
                                 seen list.  Requires seen_bits. */
+  int kernel_policy;         /* which kernel runs this call (for tests and tuning;
+                                both compute the same results):
+                                0 = automatic (kps_sample and kps_sample_seeded
+                                    always use it): the row kernel — one CTA per
+                                    row, the row read from global memory with
+                                    16-byte loads, two CTAs per SM — for batches
+                                    of at least 64 rows whose rows are 16-byte
+                                    aligned and V <= 262144; the cluster kernel —
+                                    one thread-block cluster per row, the row
+                                    resident in the cluster's shared memory —
+                                    otherwise;
+                                1 = always the cluster kernel;
+                                2 = the row kernel whenever the shape allows it;
+                                3 = as 2, with the row kernel's exact whole-row
+                                    selection forced on every row (the path it
+                                    takes when its sample misses); slow.
+                                Other values: KPS_ERR_INVALID_ARG.  The library
+                                keeps no kernel choice between calls. */
 } kps_step_opts;
 
 kps_status kps_sample_step(const void* logits, kps_dtype dt, int64_t B, int64_t V,
@@ -224,21 +242,6 @@ kps_status kps_sample_noalloc(const void* logits, kps_dtype dt, int64_t B, int64
                               const float* penalty, const float* q, float eps, int need_logits,
                               int64_t* out_idx, float* out_filtered, cudaStream_t stream);
 
-/* Kernel selection, process-wide (for tests and tuning):
- *   0 = automatic (default): the row kernel — one CTA per row, the row read
- *       from global memory with 16-byte loads, two CTAs per SM — for batches
- *       of at least 64 rows whose rows are 16-byte aligned and V <= 262144;
- *       the cluster kernel — one thread-block cluster per row, the row
- *       resident in the cluster's shared memory — otherwise;
- *   1 = always the cluster kernel;
- *   2 = the row kernel whenever the shape allows it;
- *   3 = as 2, with the row kernel's exact whole-row selection forced on
- *       every row (the path it takes when its sample misses); slow, for
- *       tests of that path.
- * Both compute the same results.  Not thread-safe against concurrent
- * kps_sample calls. */
-kps_status kps_set_kernel_policy(int policy);
-int kps_get_kernel_policy(void);
 
 /* Which kernel the most recent kps_sample call of the calling host thread
  * that launched one used: 1 = the cluster kernel (kps_sample_kernel),
@@ -250,6 +253,13 @@ int kps_last_kernel(void);
  * launched any queued: 1, or 2 when the row kernel was preceded by its
  * pre-pass over the top-p-only rows (kps_prepass_kernel); 0 = none yet. */
 int kps_last_launch_count(void);
+
+/* CTAs per thread-block cluster of the kernel that the most recent kps_sample
+ * call of the calling host thread launched (for the cluster kernel: the CTAs
+ * that share one row); 0 = none yet.  Matches the cluster_size that
+ * kps_query_launch reports for the same (B, V, dt) under the automatic policy
+ * whenever that call took the cluster kernel. */
+int kps_last_cluster_size(void);
 
 /* Static description of a status code. */
 const char* kps_status_string(kps_status s);

@@ -132,6 +132,20 @@ def test_seen_bit_options_are_checked_without_gpu(lib):
         assert lib.kps_sample_step(*args) not in (1, 3)
 
 
+def test_kernel_policy_is_per_call_and_checked(lib):
+    """The kernel choice travels with each call (kps_step_opts.kernel_policy): the library
+    exports no process-wide setter, and an unknown policy is rejected on the host."""
+    from decode_token_sampling_gb300 import StepOpts
+    assert not hasattr(lib, "kps_set_kernel_policy")
+    fake = ctypes.c_void_p(1 << 20)
+    opts = StepOpts(fake, 0, 0, 0, None, 0, None, None, 0, 7)
+    args = [fake, 0, 4, 100, fake, fake, fake, None, None, None, ctypes.byref(opts), ctypes.c_float(1e-20), 0, fake,
+            None, fake, 4096, None]
+    assert lib.kps_sample_step(*args) == 1
+    opts.kernel_policy = -1
+    assert lib.kps_sample_step(*args) == 1
+
+
 def test_step_opts_layout_matches_the_header(tmp_path):
     """The binding's kps_step_opts has the header's field offsets and size (checked by
     compiling a C program against include/kps.h)."""

@@ -507,3 +507,23 @@ def test_more_work_units_than_the_item_list_holds():
         compare(inp, ref, gi, gf, "B=80000 V=16")
     finally:
         kps.set_kernel_policy(kps.KERNEL_AUTO)
+
+
+def test_cluster_size_follows_the_batch():
+    """The launch shapes are cached per (device, dtype, V) only; the cluster kernel's width
+    still follows each call's batch size.  A call at B=40 and then one at B=1 on a 262144-token
+    bf16 vocabulary each launch the cluster size kps_query_launch reports for their own B
+    (the single row gets the widest cluster), and both match the oracle."""
+    import torch
+    import decode_token_sampling_gb300 as kps
+    kps.set_kernel_policy(kps.KERNEL_AUTO)
+    V = 262144
+    for B in (40, 1, 40):
+        inp = make_random(B, V, seed=90 + B, dtype="bf16", k_range=(1, 200), p_range=(0.5, 0.95))
+        ref = oracle.sample(inp)
+        gi, gf = run_gpu(inp)
+        compare(inp, ref, gi, gf, f"B={B} V={V}")
+        assert kps.last_kernel() == "kps_sample_kernel"
+        want = kps.query_launch(B, V, torch.bfloat16)["cluster_size"]
+        assert kps.last_cluster_size() == want, (B, kps.last_cluster_size(), want)
+    assert kps.query_launch(1, V, torch.bfloat16)["cluster_size"] > kps.query_launch(40, V, torch.bfloat16)["cluster_size"]
