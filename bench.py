@@ -58,16 +58,19 @@ def kernel_source_hash() -> str:
 
 
 def ncu_traffic_per_launch(kernel: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on this kernel source."""
-    p = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    """DRAM bytes per launch and the committed ncu summary they come from, if that summary was
+    taken on this kernel source; (None, None) otherwise.  The figure is read from the summary,
+    not measured by this run."""
+    rel = os.path.join("profiles", f"{kernel}_{workload}.md")
+    p = os.path.join(ROOT, rel)
     if not os.path.exists(p):
-        return None
+        return None, None
     txt = open(p).read()
     m_hash = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", txt)
     m_b = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", txt)
     if not m_hash or not m_b or m_hash.group(1) != kernel_source_hash():
-        return None
-    return int(m_b.group(1))
+        return None, None
+    return int(m_b.group(1)), rel
 
 
 class ClockSampler:
@@ -127,6 +130,23 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def host_cpu() -> dict:
+    """The host's CPU model and logical core count (reported beside the oracle's timing)."""
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith(("model name", "cpu model", "hardware")):
+                    model = ln.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    if model is None:
+        import platform
+        model = platform.processor() or platform.machine()
+    return {"cpu_model": model, "nproc": os.cpu_count()}
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -177,7 +197,8 @@ def run_reference(args, ws, rank):
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": workload_config(args.workload),
-        "cpu_baseline": {"value": rows_per_s, "unit": "rows/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": rows_per_s, "unit": "rows/s", "cores": 1, "kind": "oracle", "sample": sample,
+                         **host_cpu()},
         "e2e": {"value": rows_per_s, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -221,7 +242,65 @@ def cpu_baseline(args) -> dict:
             break
     t = time.perf_counter() - t0
     return {"value": reps * len(rows) / t, "unit": "rows/s", "cores": 1, "kind": "oracle",
-            "sample": f"first {len(rows)} rows of {args.workload}, repeated {reps}x ({t:.1f} s, single thread)"}
+            "sample": f"first {len(rows)} rows of {args.workload}, repeated {reps}x ({t:.1f} s, single thread)",
+            **host_cpu()}
+
+
+PER_CONFIG = ("small_mixed", "bf16_zipf", "flat_nucleus", "single_row_long", "batch256_penalty")
+
+
+def per_config_run(name: str, dev, steps: int, peak_gbs: float) -> dict:
+    """One configuration on its own: CUDA-event time of `steps` back-to-back calls (after 20
+    warm-up calls) on a side stream, its rows/s, algorithmic bytes (logits read, the filtered
+    row written when asked for, q read at the kept indices, seen ids, per-row parameters and
+    the index) and their fraction of the measured copy bandwidth."""
+    import numpy as np
+    import torch
+    import decode_token_sampling_gb300 as kps
+    from decode_token_sampling_gb300.workloads import make_workload
+    inp = make_workload(name)
+    B, V = inp.B, inp.V
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    logits = t(inp.logits) if inp.dtype == "f32" else t(inp.logits.view(np.int16)).view(torch.bfloat16)
+    top_k, top_p, temp, q = t(inp.top_k), t(inp.top_p), t(inp.temperature), t(inp.q)
+    pen = dict(seen_indptr=t(inp.seen_indptr), seen_ids=t(inp.seen_ids), penalty=t(inp.penalty)) \
+        if inp.seen_indptr is not None else {}
+    out_idx = torch.empty(B, dtype=torch.int64, device=dev)
+    out_f = torch.empty(B, V, dtype=torch.float32, device=dev) if inp.need_logits else None
+    wsp = kps.new_workspace(B, V, logits.dtype, dev)
+    stream = torch.cuda.Stream(dev)
+    call = lambda: kps.sample(logits, top_k, top_p, temp, q, eps=inp.eps, need_logits=inp.need_logits,
+                              out_idx=out_idx, out_filtered=out_f, workspace=wsp, stream=stream, **pen)
+    with torch.cuda.stream(stream):
+        for _ in range(20):
+            call()
+    stream.synchronize()
+    kernel = kps.last_kernel()
+    if kps.last_launch_count() == 2:
+        kernel = "kps_prepass_kernel+" + kernel
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        call()
+    e1.record(stream)
+    stream.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    if kps.last_device_status(wsp, stream) != 0:
+        raise RuntimeError(f"device status after {name}")
+    _, f_all = kps.sample(logits, top_k, top_p, temp, q, eps=inp.eps, need_logits=True, workspace=wsp, **pen)
+    kept = int((f_all != float("-inf")).sum().item())
+    del f_all
+    esize = 4 if inp.dtype == "f32" else 2
+    nnz = int(inp.seen_ids.size) if pen else 0
+    alg = (B * V * esize + (B * V * 4 if inp.need_logits else 0) + kept * 4 + nnz * 4
+           + B * (4 * 4 + 8 + (4 if nnz else 0)))
+    gbs = alg / (ms / 1e3) / 1e9
+    return {"ms_per_step": ms, "steps": steps, "rows_per_s": B / (ms / 1e3), "tokens_per_s": B / (ms / 1e3),
+            "algorithmic_bytes": alg, "achieved_gbs": gbs, "frac": gbs / peak_gbs, "peak_gbs": peak_gbs,
+            "metric_bytes": inp.metric_bytes(), "metric_gbs": inp.metric_bytes() / (ms / 1e3) / 1e9,
+            "kernel": kernel, "B": B, "V": V, "dtype": inp.dtype, "need_logits": bool(inp.need_logits),
+            "l2": "inputs exceed the 129 MB L2" if inp.metric_bytes() > 129e6 else
+                  "inputs fit the 129 MB L2 (back-to-back calls find them there)"}
 
 
 def main():
@@ -243,6 +322,8 @@ def main():
                          "kept on the device, the step setting each emitted token's bit (kps_sample_step)")
     ap.add_argument("--kernel", default="auto", choices=["auto", "cluster", "row"],
                     help="kernel policy (auto picks per shape; both compute the same results)")
+    ap.add_argument("--per-config-steps", type=int, default=300,
+                    help="steps timed for each configuration of the per_config report (0: no report)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -361,7 +442,7 @@ def main():
     achieved_gbs = alg_bytes / (kernel_ms / 1e3) / 1e9
     # the committed capture is of the default inputs (supplied draws, seen id lists)
     default_inputs = args.draws == "supplied" and not bits_kw
-    traffic = ncu_traffic_per_launch(kernel_name, args.workload) if default_inputs else None
+    traffic, traffic_src = ncu_traffic_per_launch(kernel_name, args.workload) if default_inputs else (None, None)
 
     # ---- end to end through the public API: pinned host inputs in, results out ---------------
     # Every step copies its inputs from pinned host memory, samples, and copies its results
@@ -454,9 +535,13 @@ def main():
         "gpu_launches": args.steps * launches_per_step,
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": traffic,
+                     "traffic_source": traffic_src or "none: no committed ncu summary of this kernel source",
                      "peak_source": peaks["source"], "kernel": kernel_name,
                      "algorithmic_bytes_per_launch": alg_bytes, "kernel_ms": kernel_ms},
     }
+    if rank == 0 and ws == 1 and args.per_config_steps > 0:
+        line["per_config"] = {name: per_config_run(name, dev, max(args.per_config_steps, 200), peaks["hbm_gbs"])
+                              for name in PER_CONFIG if name != args.workload}
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args)
     if rank == 0:
