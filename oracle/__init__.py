@@ -51,6 +51,9 @@ def _load() -> ctypes.CDLL:
         lib.kpso_philox4x32_10.argtypes = [P, ctypes.c_uint32, ctypes.c_uint32]
         lib.kpso_seen_ids_from_bits.restype = ctypes.c_int64
         lib.kpso_seen_ids_from_bits.argtypes = [P, ctypes.c_int64, ctypes.c_int64, P, P]
+        lib.kpso_row_terms.restype = ctypes.c_int64
+        lib.kpso_row_terms.argtypes = [P, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, P, P, P, P,
+                                       P, P, P, P, P, P]
         lib.kpso_seen_append.restype = None
         lib.kpso_seen_append.argtypes = [P, P, ctypes.c_int64, ctypes.c_int64]
         _lib = lib
@@ -102,6 +105,34 @@ def sample(inp, need_logits: Optional[bool] = None) -> dict:
     nl = inp.need_logits if need_logits is None else need_logits
     return sample_arrays(inp.logits, inp.dtype, inp.top_k, inp.top_p, inp.temperature, inp.q, inp.eps,
                          nl, inp.seen_indptr, inp.seen_ids, inp.penalty)
+
+
+def row_terms(inp, b: int) -> dict:
+    """The terms of row b of a workloads.SamplingInputs before top-p: the transformed row x
+    (float32 [V]: NaN -> -inf, penalty, temperature), the first nK elements of the order pi
+    (int64), their softmax weights e (float64, e = exp(x - max)), their sum S, and whether
+    the row is greedy.  For checking a result at a near-tie against the definition."""
+    lib = _load()
+    logits = np.ascontiguousarray(inp.logits, dtype=np.float32 if inp.dtype == "f32" else np.uint16)
+    B, V = logits.shape
+    top_k = np.ascontiguousarray(inp.top_k, dtype=np.int32)
+    temperature = np.ascontiguousarray(inp.temperature, dtype=np.float32)
+    indptr = ids = pen = None
+    if inp.seen_indptr is not None:
+        indptr = np.ascontiguousarray(inp.seen_indptr, dtype=np.int32)
+        ids = np.ascontiguousarray(inp.seen_ids, dtype=np.int32)
+        pen = np.ascontiguousarray(inp.penalty, dtype=np.float32)
+    x = np.empty(V, np.float32)
+    order = np.empty(V, np.int64)
+    e = np.empty(V, np.float64)
+    S = np.zeros(1, np.float64)
+    greedy = np.zeros(1, np.int32)
+    nK = lib.kpso_row_terms(_ptr(logits), 0 if inp.dtype == "f32" else 1, B, V, int(b), _ptr(top_k),
+                            _ptr(temperature), _ptr(indptr), _ptr(ids), _ptr(pen), _ptr(x), _ptr(order), _ptr(e),
+                            _ptr(S), _ptr(greedy))
+    if nK < 1:
+        raise ValueError(f"oracle rejected its arguments (code {nK})")
+    return dict(x=x, order=order[:nK].copy(), e=e[:nK].copy(), S=float(S[0]), nK=int(nK), greedy=bool(greedy[0]))
 
 
 def exp_draws(B: int, V: int, seed: int, step: int = 0) -> np.ndarray:

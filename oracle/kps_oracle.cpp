@@ -70,10 +70,21 @@ struct RowResult {
   double topp_gap;  // distance of the deciding cumsums from p*S, relative to p*S
 };
 
-RowResult sample_row(std::vector<float>& x, int64_t V, int32_t k, float p, float T,
-                     const int32_t* ids, int64_t nids, bool pen_on, float pen,
-                     const float* qrow, float eps, float* out_row) {
+// The row's terms up to the top-k set: the transformed row x (NaN -> -inf, penalty,
+// temperature), the order pi restricted to its first nK elements, their softmax weights
+// e and the sum S.
+struct RowTerms {
+  bool greedy;
+  int64_t nK;
+  std::vector<int64_t> order;  // order[0 .. nK) sorted under pi
+  std::vector<double> e;       // e[i] = exp(x[order[i]] - M), i < nK
+  double S;
+};
+
+RowTerms row_terms(std::vector<float>& x, int64_t V, int32_t k, float T,
+                   const int32_t* ids, int64_t nids, bool pen_on, float pen) {
   const float NEG_INF = -std::numeric_limits<float>::infinity();
+  RowTerms t;
 
   // NaN logits are treated as -inf.
   for (int64_t v = 0; v < V; ++v)
@@ -92,15 +103,16 @@ RowResult sample_row(std::vector<float>& x, int64_t V, int32_t k, float p, float
   }
 
   // Temperature [MM10 §10.4]: x / T, or greedy when T is not finite and positive.
-  const bool greedy = !(T > 0.0f) || std::isinf(T);
-  if (!greedy)
+  t.greedy = !(T > 0.0f) || std::isinf(T);
+  if (!t.greedy)
     for (int64_t v = 0; v < V; ++v) x[v] = x[v] / T;
 
   // Total order pi: value descending, index ascending.
   auto before = [&x](int64_t a, int64_t b) {
     return x[a] > x[b] || (x[a] == x[b] && a < b);
   };
-  std::vector<int64_t> order(static_cast<size_t>(V));
+  std::vector<int64_t>& order = t.order;
+  order.resize(static_cast<size_t>(V));
   for (int64_t v = 0; v < V; ++v) order[v] = v;
 
   // Top-k [NPU topK item 2; MM10 §10.5]: exactly the first k under pi.
@@ -113,16 +125,32 @@ RowResult sample_row(std::vector<float>& x, int64_t V, int32_t k, float p, float
   } else {
     std::sort(order.begin(), order.end(), before);
   }
+  t.nK = nK;
 
   // Softmax over K in double [CPP softmax; NPU topK softmax step].
   const double M = static_cast<double>(x[order[0]]);
-  std::vector<double> e(static_cast<size_t>(nK));
+  std::vector<double>& e = t.e;
+  e.resize(static_cast<size_t>(nK));
   double S = 0.0;
   for (int64_t i = 0; i < nK; ++i) {
     double xv = static_cast<double>(x[order[i]]);
     e[i] = (xv == M) ? 1.0 : std::exp(xv - M);
     S += e[i];
   }
+  t.S = S;
+  return t;
+}
+
+RowResult sample_row(std::vector<float>& x, int64_t V, int32_t k, float p, float T,
+                     const int32_t* ids, int64_t nids, bool pen_on, float pen,
+                     const float* qrow, float eps, float* out_row) {
+  const float NEG_INF = -std::numeric_limits<float>::infinity();
+  const RowTerms t = row_terms(x, V, k, T, ids, nids, pen_on, pen);
+  const bool greedy = t.greedy;
+  const int64_t nK = t.nK;
+  const std::vector<int64_t>& order = t.order;
+  const std::vector<double>& e = t.e;
+  const double S = t.S;
 
   // Top-p [NPU topP fallback; MM10 §10.6; CPP top_p].
   int64_t nP = nK;
@@ -230,6 +258,47 @@ int kpso_sample(const void* logits, int dtype, int64_t B, int64_t V,
     if (out_topp_gap) out_topp_gap[b] = r.topp_gap;
   }
   return 0;
+}
+
+// The terms of row b (for checking a result at a near-tie against the definition rather
+// than against this oracle's own choice): the transformed row x_out[V], the first nK
+// elements of the order pi in order_out, their weights e_out and S.  order_out and e_out
+// hold V entries.  Returns nK (>= 1), or -1 on an invalid argument; *greedy_out is 1 for
+// a greedy row.
+int64_t kpso_row_terms(const void* logits, int dtype, int64_t B, int64_t V, int64_t b,
+                       const int32_t* top_k, const float* temperature,
+                       const int32_t* seen_indptr, const int32_t* seen_ids, const float* penalty,
+                       float* x_out, int64_t* order_out, double* e_out, double* S_out,
+                       int* greedy_out) {
+  if (b < 0 || b >= B || V < 1 || !logits || !top_k || !temperature || !x_out || !order_out ||
+      !e_out || !S_out || !greedy_out)
+    return -1;
+  if (dtype != 0 && dtype != 1) return -1;
+  std::vector<float> x(static_cast<size_t>(V));
+  if (dtype == 0) {
+    const float* row = static_cast<const float*>(logits) + b * V;
+    for (int64_t v = 0; v < V; ++v) x[v] = row[v];
+  } else {
+    const uint16_t* row = static_cast<const uint16_t*>(logits) + b * V;
+    for (int64_t v = 0; v < V; ++v) x[v] = bf16_bits_to_float(row[v]);
+  }
+  bool pen_on = seen_indptr && seen_ids && penalty && (penalty[b] > 0.0f);
+  const int32_t* ids = nullptr;
+  int64_t nids = 0;
+  if (pen_on) {
+    ids = seen_ids + seen_indptr[b];
+    nids = static_cast<int64_t>(seen_indptr[b + 1]) - seen_indptr[b];
+    if (nids < 0) nids = 0;
+  }
+  const RowTerms t = row_terms(x, V, top_k[b], temperature[b], ids, nids, pen_on, pen_on ? penalty[b] : 1.0f);
+  for (int64_t v = 0; v < V; ++v) x_out[v] = x[v];
+  for (int64_t i = 0; i < t.nK; ++i) {
+    order_out[i] = t.order[i];
+    e_out[i] = t.e[i];
+  }
+  *S_out = t.S;
+  *greedy_out = t.greedy ? 1 : 0;
+  return t.nK;
 }
 
 // ---- Exp(1) draws from a counter-based generator (sampling without a supplied q) ---------

@@ -8,3 +8,26 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Near-tie rows per test: how many rows each parity comparison found within 1e-6 of a
+    race or top-p tie, and how many of those differed from the oracle's choice and were
+    accepted on validity against the definition instead."""
+    parity = sys.modules.get("parity")
+    log = getattr(parity, "NEAR_LOG", None)
+    if not log:
+        return
+    per = {}
+    for test, _label, rows, near, acc in log:
+        t = per.setdefault(test, [0, 0, 0, 0])
+        t[0] += 1
+        t[1] += rows
+        t[2] += near
+        t[3] += acc
+    tr = terminalreporter
+    tr.section("near-tie rows (compared / near a tie / accepted on validity)")
+    for test, (calls, rows, near, acc) in sorted(per.items()):
+        tr.write_line(f"{test}: {calls} comparisons, {rows} rows, {near} near, {acc} accepted")
+    tot = [sum(v[i] for v in per.values()) for i in range(4)]
+    tr.write_line(f"total: {tot[0]} comparisons, {tot[1]} rows, {tot[2]} near, {tot[3]} accepted")
