@@ -32,19 +32,32 @@ def nvcc() -> str:
     return cand
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None) -> str:
-    """Compile libkps.so if it is missing or older than its sources; returns its path."""
+def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None,
+          out: str = LIB) -> str:
+    """Compile libkps.so (or, with extra_flags and another `out`, a variant of it) if it is
+    missing or older than its sources; returns its path."""
     srcs = [HDR] + [os.path.join(PKG, "csrc", f) for f in sorted(os.listdir(os.path.join(PKG, "csrc")))
                     if f.endswith((".cu", ".cuh", ".h"))]
-    if not force and os.path.exists(LIB) and all(os.path.getmtime(LIB) >= os.path.getmtime(s) for s in srcs):
-        return LIB
-    tmp = LIB + f".tmp{os.getpid()}"
+    if not force and os.path.exists(out) and all(os.path.getmtime(out) >= os.path.getmtime(s) for s in srcs):
+        return out
+    tmp = out + f".tmp{os.getpid()}"
     cmd = [nvcc(), *NVCC_FLAGS, *(extra_flags or []), "-I", os.path.join(ROOT, "include"), "-o", tmp, SRC]
     if verbose:
         print(" ".join(cmd))
     subprocess.check_call(cmd)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, out)
+    return out
+
+
+# Test-only variant: the cluster kernel's first copy wait in each CTA goes to a barrier that
+# no copy completes, bounded by this many clock cycles, so that its timeout path (status
+# KPS_ERR_TIMEOUT, one more bounded wait for the real copy) runs on every call.
+SPIN_TEST_LIB = os.path.join(PKG, "libkps_spin_test.so")
+SPIN_TEST_CYCLES = 20000
+
+
+def build_spin_test(force: bool = False) -> str:
+    return build(force=force, extra_flags=[f"-DKPS_TEST_SPIN_CYCLES={SPIN_TEST_CYCLES}LL"], out=SPIN_TEST_LIB)
 
 
 if __name__ == "__main__":

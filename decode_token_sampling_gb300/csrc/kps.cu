@@ -44,13 +44,17 @@
 // histograms and small exact rankings instead of the sorts and quickselects
 // on those pages.
 //
-// Nothing here waits without a bound: the TMA wait gives up after ~2 s of
-// clock cycles, records KPS_ERR_TIMEOUT in the status word and carries on
-// with the same control flow, so the cluster barriers always complete.
+// Nothing here waits without a bound: a TMA wait that gives up after ~2 s of
+// clock cycles records KPS_ERR_TIMEOUT in the status word and gives the copy
+// one more bound before its buffer is read or reused; a copy still out after
+// that stops all further copies of the CTA, which carries on with the same
+// control flow (so the cluster barriers always complete) and waits for it once
+// more before it exits.
 
 #include "kps.h"
 #include "kps_fixed.h"
 #include "kps_div.h"
+#include "kps_weights.cuh"
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -300,15 +304,6 @@ __device__ __forceinline__ void seen_append(const Params& P, int64_t row, long l
   atomicOr(P.seen_bits + row * seen_words(P.V) + (tok >> 5), 1u << (tok & 31));
 }
 
-__device__ __forceinline__ float softmax_weight(float x, float M) {
-  if (x == M) return 1.0f;
-  float s = __fsub_rn(x, M);
-  if (!(s > -INFINITY)) return 0.0f;
-  float bb = __fsub_rn(s, x);
-  float lo = __fadd_rn(__fsub_rn(x, __fsub_rn(s, bb)), __fsub_rn(-M, bb));
-  float e = expf(s);
-  return __fmaf_rn(e, lo, e);
-}
 __device__ __forceinline__ unsigned long long fixed_mass(float w) {
   return fixed_mass_of(w);
 }
@@ -374,11 +369,12 @@ __device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t 
       : "memory");
   return ok != 0;
 }
-// Bounded wait: returns false if the phase did not complete within kSpinCycles.
-__device__ __forceinline__ bool mbar_wait_bounded(unsigned long long* bar, uint32_t parity) {
+// Bounded wait: returns false if the phase did not complete within `cycles`.
+__device__ __forceinline__ bool mbar_wait_bounded(unsigned long long* bar, uint32_t parity,
+                                                  long long cycles = kSpinCycles) {
   long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > kSpinCycles) return false;
+    if (clock64() - t0 > cycles) return false;
   }
   return true;
 }
@@ -1029,8 +1025,12 @@ __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P)
   auto gsrc_of = [&](int64_t row) {
     return static_cast<const unsigned char*>(P.logits) + (row * V + c0) * esize;
   };
+  // dead: a copy of this CTA did not land within two bounds; no further copies are issued
+  // (block-uniform, decided by a barrier vote)
+  bool dead = false;
+  uint32_t dead_parity = 0;
   auto issue_load = [&](int64_t row) {
-    if (tma && threadIdx.x == 0) {
+    if (tma && !dead && threadIdx.x == 0) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       mbar_expect_tx(mbar, bytes);
       // one bulk copy per chunk: a copy's cost is mostly fixed, not proportional to its size
@@ -1056,9 +1056,13 @@ __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P)
   };
 
   if (threadIdx.x == 0) mbar_init(mbar, 1);
+#ifdef KPS_TEST_SPIN_CYCLES
+  // test build: the first wait goes to a second barrier that no copy completes, with a
+  // bound of KPS_TEST_SPIN_CYCLES, so that the timeout path below runs deterministically
+  if (threadIdx.x == 0) mbar_init(mbar + 1, 1);
+#endif
   __syncthreads();
   if (my_rows > 0) issue_load(row_at(0));
-  bool timed_out = false;
   uint32_t parity = 0;
 
   for (int ri = 0; ri < my_rows; ++ri, parity ^= 1u) {
@@ -1114,10 +1118,21 @@ __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P)
         if (kBF16) xs[i] = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(src)[i]);
         else xs[i] = reinterpret_cast<const float*>(src)[i];
       }
-    } else {
-      if (!mbar_wait_bounded(mbar, parity)) {
-        timed_out = true;
+    } else if (!dead) {
+#ifdef KPS_TEST_SPIN_CYCLES
+      const bool ok = ri == 0 ? mbar_wait_bounded(mbar + 1, 0u, KPS_TEST_SPIN_CYCLES) : mbar_wait_bounded(mbar, parity);
+#else
+      const bool ok = mbar_wait_bounded(mbar, parity);
+#endif
+      if (__syncthreads_or(!ok)) {
+        // the copy did not land in time: report it, and give it one more bound before its
+        // buffer is read (or reused by the next row's copy)
         if (threadIdx.x == 0) atomicMax(P.status, kStatusTimeout);
+        const bool late = mbar_wait_bounded(mbar, parity);
+        if (__syncthreads_or(!late)) {
+          dead = true;
+          dead_parity = parity;
+        }
       }
       if (kBF16) {
         const __nv_bfloat16* raw = reinterpret_cast<const __nv_bfloat16*>(smem + L.raw);
@@ -1625,8 +1640,8 @@ __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P)
     if (!next_issued && next >= 0) issue_load(next);
   }
 
-  // a CTA that gave up on a copy waits (bounded) for it before leaving
-  if (timed_out) (void)mbar_wait_bounded(mbar, parity);
+  // a CTA that gave up on a copy waits (bounded) for it once more before leaving
+  if (dead) (void)mbar_wait_bounded(mbar, dead_parity);
   // no CTA leaves while another may still read its shared memory
   cl.sync();
 }

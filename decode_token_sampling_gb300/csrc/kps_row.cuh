@@ -120,14 +120,6 @@ __device__ __forceinline__ void unpack16(const uint4 w, float* v) {
   }
 }
 
-// 1/x to about one ulp (the hardware approximation): race quotients only decide near-ties
-// differently from the exact ones.
-__device__ __forceinline__ float rrcp_approx(float x) {
-  float r;
-  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
-  return r;
-}
-
 // Shared-memory add without a return value (the pointer must address shared memory).
 __device__ __forceinline__ void sh_red_add(uint32_t* p, uint32_t v) {
   asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
@@ -1284,14 +1276,7 @@ __device__ __noinline__ int32_t rrow_first_max(const RowCtx& rc, float M, unsign
 
 constexpr int kRPBins = 2048;           // mass bins of top-p-only rows: width 1/32 below H
 constexpr float kRPScale = 32.0f;
-
-// 2^x to about 2^-22 relative (the hardware approximation).
-__device__ __forceinline__ float rex2(float x) {
-  float r;
-  asm("ex2.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
-  return r;
-}
-constexpr float kLog2e = 1.4426950408889634f;
+static_assert(kRPBins == kExpBins, "one bin factor per mass bin");
 
 // The reference H of a top-p-only row lies on the 1/32 grid (rounded up) with |H| < 2^18,
 // so every bin top H - b/32 (b < 2048) is a float exactly.  Rows whose H cannot (an
@@ -1301,28 +1286,17 @@ __device__ __forceinline__ float pgrid_up(float h) {
 }
 __device__ __forceinline__ bool pgrid_ok(float h) { return fabsf(h) < 262144.0f; }  // false for NaN, inf
 
-// The bin factor exp(-b/32), to about 2^-22 relative: its base-2 exponent b log2(e) / 32
-// is split into an integer and a fraction with log2(e) / 32 carried as an 11-bit head
-// (whose product with b < 2^11 is exact) plus a tail, so the error does not grow with b.
-__device__ __forceinline__ float pfac(int b) {
-  constexpr float kHead = 0.045074462890625f;        // log2(e) / 32 to 12 bits (1477 / 2^15)
-  constexpr float kTail = 9.757137155105844e-06f;     // log2(e) / 32 - kHead
-  const float fb = static_cast<float>(b);
-  const float zh = __fmul_rn(fb, kHead);             // exact
-  const float n = floorf(zh);
-  const float frac = __fmaf_rn(fb, kTail, __fsub_rn(zh, n));  // in [0, 1.02)
-  return __fmul_rn(rex2(-frac), __int_as_float((127 - static_cast<int>(n)) << 23));
-}
-
 // The weight of y against the reference H (on the grid, H >= y): its bin
-// b = floor(32 fl(H - y)) (kRPBins when that is not in [0, 2048): no mass) and the weight
-// relative to the bin top c = H - b/32 (exact), exp(-(c - y)) as an integer w24 in units
-// of 2^-24 (c - y is exact to 2^-30, so the only error is the exponential's, about 2^-22
-// relative; the top weight 2^24 is clamped to 2^24 - 1).  The mass of an element is
-// w24 * 2^-24 * exp(-b/32) against exp(H); every total, prefix and race below is taken in
-// this one arithmetic, so they agree with each other exactly.  The bin comes from the
-// rounded difference, so an element near a bin edge may fall on either side; its weight
-// follows its bin, and both passes see the same bin.
+// b = floor(32 (H - y)) of the exact difference, i.e. H - (b + 1)/32 < y <= H - b/32
+// (kRPBins when b is not in [0, 2048): no mass), and the weight relative to the bin top
+// c = H - b/32 (exact), exp(-(c - y)) as an integer w24 in units of 2^-24 (w24_weight;
+// c - y is exact to 2^-30, so the error is the exponential's).  The mass of an element is
+// w24 * 2^-24 * exp(-b/32) against exp(H), with exp(-b/32) from the table kExpBin; every
+// total, prefix and race below is taken in this one arithmetic, so they agree with each
+// other exactly.  The bin is first taken from the rounded difference fl(H - y), which may
+// lie across a bin edge from the exact one; comparing y with the exact bin edges then
+// moves it to the bin of the exact difference, so bins order the elements exactly and pass
+// B can classify them by comparing y with the same edges.
 struct PW {
   int b;
   uint32_t w24;
@@ -1332,10 +1306,19 @@ struct PW {
 __device__ __forceinline__ PW pweight(float y, float H) {
   const float d = __fsub_rn(H, y);
   const float t = __fmaf_rd(d, kRPScale, 8388608.0f);  // floor(32 d) + 2^23 (exact product)
-  const uint32_t bu = __float_as_uint(t) - 0x4B000000u;
-  const float c = __fmaf_rn(__fsub_rn(t, 8388608.0f), -1.0f / kRPScale, H);
+  uint32_t bu = __float_as_uint(t) - 0x4B000000u;
+  float c = __fmaf_rn(__fsub_rn(t, 8388608.0f), -1.0f / kRPScale, H);  // H - b/32, exact
+  // to the bin of the exact difference (c and c -+ 1/32 are exact; one step suffices, as
+  // fl(H - y) is within 2^-19 of H - y below the last bin edge)
+  if (y > c) {
+    c = __fadd_rn(c, 1.0f / kRPScale);
+    --bu;
+  } else if (y <= __fsub_rn(c, 1.0f / kRPScale)) {
+    c = __fsub_rn(c, 1.0f / kRPScale);
+    ++bu;
+  }
   const float frac = __fsub_rn(c, y);
-  const float v = fminf(rex2(__fmaf_rn(frac, -kLog2e, 24.0f)), 16777215.0f);  // an integer in [2^23, 2^24)
+  const float v = w24_weight(frac);  // an integer in [2^23, 2^24)
   PW r;
   r.b = bu < static_cast<uint32_t>(kRPBins) ? static_cast<int>(bu) : kRPBins;
   r.w24 = __float_as_uint(v) - 0x4A800000u;
@@ -1352,7 +1335,7 @@ __device__ __forceinline__ int psub(const PW& w) {
 }
 
 // Race quotient of an element of a top-p-only row before its bin factor: its weight
-// w24 / (q + eps) (reciprocal to about one ulp), as a key that is 0 for NaN or a negative
+// w24 / (q + eps) (by the approximate reciprocal), as a key that is 0 for NaN or a negative
 // quotient and otherwise orders like the quotient.  The full quotient is this times
 // 2^-24 exp(-b/32), rounded once more, so the best of a bin is the bin's best key.
 __device__ __forceinline__ uint32_t prace_key(float wf, float q, float eps) {
@@ -1476,10 +1459,11 @@ __device__ __noinline__ uint32_t rp_pass_b(const RowCtx& rc, float H, int bstar,
   const bool pen_on = rc.pen_on, identity = rc.identity;
   const float pen = rc.pen;
   const FixedDivisor dv = rc.div;
-  // bin b = floor(32 d) with d = fl(H - y) is taken on an exact multiple of d, so
-  // b < bstar exactly when d < bstar / 32
-  const float clo = static_cast<float>(bstar) * (1.0f / kRPScale);
-  const float chi = bstar < kRPBins ? static_cast<float>(bstar + 1) * (1.0f / kRPScale) : clo;
+  // bin b holds H - (b + 1)/32 < y <= H - b/32 (pweight), so y is kept (b < bstar) exactly
+  // when y > H - bstar/32 and in the band (b = bstar) when not kept and y > H - (bstar + 1)/32
+  // (both edges exact floats)
+  const float ykeep = __fmaf_rn(static_cast<float>(bstar), -1.0f / kRPScale, H);
+  const float yband = bstar < kRPBins ? __fmaf_rn(static_cast<float>(bstar + 1), -1.0f / kRPScale, H) : ykeep;
   uint32_t wcnt = 0;
   for (int base = g0; base < g1; base += kRT * kUB) {
     uint4 w[kUB];
@@ -1504,9 +1488,8 @@ __device__ __noinline__ uint32_t rp_pass_b(const RowCtx& rc, float H, int bstar,
 #pragma unroll
       for (int e = 0; e < G; ++e) {
         v[e] = __fadd_rn(identity ? v[e] : rdiv(v[e], dv), 0.0f);  // NaN: neither kept nor in the band
-        const float d = __fsub_rn(H, v[e]);
-        kmask |= (in && d < clo ? 1u : 0u) << e;
-        bmask |= (in && d >= clo && d < chi ? 1u : 0u) << e;
+        kmask |= (in && v[e] > ykeep ? 1u : 0u) << e;
+        bmask |= (in && v[e] <= ykeep && v[e] > yband ? 1u : 0u) << e;
       }
       if (__any_sync(kFull, bmask != 0u)) {
 #pragma unroll
@@ -1684,7 +1667,7 @@ __device__ __noinline__ int32_t rwide_row(const RowCtx& rc, const RowSmem& sm, c
   // bin factors exp(-b/32), the bin masses summed over the members, their total S, and
   // the bin bstar holding the boundary (its prefix reaches p * S)
   float* ftab = reinterpret_cast<float*>(sm.wbuf);
-  for (int b = threadIdx.x; b < kRPBins; b += kRT) ftab[b] = pfac(b);
+  for (int b = threadIdx.x; b < kRPBins; b += kRT) ftab[b] = kExpBin.v[b];
   double above = 0.0, tq = 0.0;
   int bstar;
   unsigned long long ubest[kRPBins / kRT];  // the best race word of each of this thread's bins
@@ -1708,7 +1691,7 @@ __device__ __noinline__ int32_t rwide_row(const RowCtx& rc, const RowSmem& sm, c
         }
       }
       ubest[e] = wb;
-      m[e] = static_cast<double>(c) * 5.9604644775390625e-8 * static_cast<double>(pfac(b));
+      m[e] = static_cast<double>(c) * 5.9604644775390625e-8 * static_cast<double>(kExpBin.v[b]);
       sum += m[e];
     }
     if (threadIdx.x == 0) sm.misc[kMBin] = static_cast<unsigned long long>(kRPBins);
