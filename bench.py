@@ -130,17 +130,30 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+_ARM_PARTS = {"0xd4f": "Neoverse V2", "0xd40": "Neoverse V1", "0xd49": "Neoverse N2", "0xd0c": "Neoverse N1"}
+
+
 def host_cpu() -> dict:
-    """The host's CPU model and logical core count (reported beside the oracle's timing)."""
+    """The host's CPU model and logical core count (reported beside the oracle's timing).
+    x86 hosts name the model in /proc/cpuinfo; Arm hosts give an implementer and part code."""
     model = None
+    impl = part = None
     try:
         with open("/proc/cpuinfo") as f:
             for ln in f:
-                if ln.lower().startswith(("model name", "cpu model", "hardware")):
-                    model = ln.split(":", 1)[1].strip()
-                    break
+                key = ln.split(":", 1)[0].strip().lower()
+                val = ln.split(":", 1)[1].strip() if ":" in ln else ""
+                if key in ("model name", "cpu model", "hardware") and model is None:
+                    model = val
+                elif key == "cpu implementer" and impl is None:
+                    impl = val
+                elif key == "cpu part" and part is None:
+                    part = val
     except OSError:
         pass
+    if model is None and part is not None:
+        name = _ARM_PARTS.get(part.lower()) if impl == "0x41" else None
+        model = f"{name} (Arm implementer {impl}, part {part})" if name else f"Arm implementer {impl}, part {part}"
     if model is None:
         import platform
         model = platform.processor() or platform.machine()
@@ -250,8 +263,9 @@ PER_CONFIG = ("small_mixed", "bf16_zipf", "flat_nucleus", "single_row_long", "ba
 
 
 def per_config_run(name: str, dev, steps: int, peak_gbs: float) -> dict:
-    """One configuration on its own: CUDA-event time of `steps` back-to-back calls (after 20
-    warm-up calls) on a side stream, its rows/s, algorithmic bytes (logits read, the filtered
+    """One configuration on its own: CUDA-event time per call of `steps` back-to-back calls
+    (after 20 warm-up calls) on a side stream, replayed from a CUDA graph (and, for
+    comparison, issued one by one through the Python binding), its rows/s, algorithmic bytes (logits read, the filtered
     row written when asked for, q read at the kept indices, seen ids, per-row parameters and
     the index) and their fraction of the measured copy bandwidth."""
     import numpy as np
@@ -279,12 +293,30 @@ def per_config_run(name: str, dev, steps: int, peak_gbs: float) -> dict:
     if kps.last_launch_count() == 2:
         kernel = "kps_prepass_kernel+" + kernel
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # eager: every call through the Python binding (at small shapes the host's marshalling,
+    # not the GPU, sets this pace)
     e0.record(stream)
     for _ in range(steps):
         call()
     e1.record(stream)
     stream.synchronize()
-    ms = e0.elapsed_time(e1) / steps
+    ms_eager = e0.elapsed_time(e1) / steps
+    # device-resident: the calls captured once in a CUDA graph and replayed, as a serving
+    # loop that captures its decode step runs them
+    per_graph = 20
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for _ in range(per_graph):
+            call()
+    replays = max(1, steps // per_graph)
+    with torch.cuda.stream(stream):
+        graph.replay()
+        e0.record(stream)
+        for _ in range(replays):
+            graph.replay()
+        e1.record(stream)
+    stream.synchronize()
+    ms = e0.elapsed_time(e1) / (replays * per_graph)
     if kps.last_device_status(wsp, stream) != 0:
         raise RuntimeError(f"device status after {name}")
     _, f_all = kps.sample(logits, top_k, top_p, temp, q, eps=inp.eps, need_logits=True, workspace=wsp, **pen)
@@ -295,7 +327,9 @@ def per_config_run(name: str, dev, steps: int, peak_gbs: float) -> dict:
     alg = (B * V * esize + (B * V * 4 if inp.need_logits else 0) + kept * 4 + nnz * 4
            + B * (4 * 4 + 8 + (4 if nnz else 0)))
     gbs = alg / (ms / 1e3) / 1e9
-    return {"ms_per_step": ms, "steps": steps, "rows_per_s": B / (ms / 1e3), "tokens_per_s": B / (ms / 1e3),
+    return {"ms_per_step": ms, "steps": replays * per_graph, "timing": f"CUDA graph of {per_graph} calls, replayed",
+            "ms_per_step_eager": ms_eager, "steps_eager": steps,
+            "rows_per_s": B / (ms / 1e3), "tokens_per_s": B / (ms / 1e3),
             "algorithmic_bytes": alg, "achieved_gbs": gbs, "frac": gbs / peak_gbs, "peak_gbs": peak_gbs,
             "metric_bytes": inp.metric_bytes(), "metric_gbs": inp.metric_bytes() / (ms / 1e3) / 1e9,
             "kernel": kernel, "B": B, "V": V, "dtype": inp.dtype, "need_logits": bool(inp.need_logits),
