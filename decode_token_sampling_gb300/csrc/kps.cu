@@ -79,6 +79,7 @@ constexpr int kSuper = 16;          // super-bins of 16 bins each (fallback radi
 constexpr int kTopKMax = 1024;      // top-k is active for 1 <= k <= min(V, 1024)
 constexpr int kCapLoc = 1024;       // candidates one CTA may hold
 constexpr int kGallCap = 2048;      // group maxima one row may have for the top-k bound
+constexpr int kGroupSplit = 8;      // groups of 128 elements split up to 8 ways (16 elements)
 constexpr int kLinBins = 2048;      // linear count bins of the top-k candidate pass
 constexpr int kLinBinsP = 1024;     // linear mass bins (width 1/16 of d = max - x) of top-p-only rows
 constexpr int kFineBins = 1024;     // linear bins of the refinement histogram (top-p-only rows)
@@ -209,7 +210,7 @@ __host__ __device__ inline Layout make_layout(int nc, bool bf16) {
   L.fine = off;     off += size_t(3 * kFineBins) * 4;
   L.sup = off;      off += size_t(kLinBinsP / 32 + kFineBins / 32) * 8;
   L.small = off;    off += size_t(2 * kSmall) * 8;  // own boundary list, then the gathered one
-  L.gmax = off;     off += align16(size_t((nc + 127) / 128) * 4);
+  L.gmax = off;     off += align16(size_t((nc + 127) / 128) * 4 * kGroupSplit);
   L.red = off;      off += 40 * 8;
   L.slots = off;    off += size_t(kNumSlots) * 8;
   L.mbar = off;     off += 16;
@@ -644,7 +645,7 @@ __device__ int32_t nth_tie(const SrcCand& s, const Ctx& c, uint32_t tkey, uint32
 // the threshold of the selected prefix.  Every CTA computes the same answer.
 // Used when the fast paths' small structures overflow.
 template <class Src, bool kMass>
-__device__ Thresh radix_select(cg::cluster_group& cl, Ctx& c, const Src& src, unsigned long long target,
+__device__ __noinline__ Thresh radix_select(cg::cluster_group& cl, Ctx& c, const Src& src, unsigned long long target,
                                bool p_mode, float p, uint32_t rk, int32_t ri) {
   constexpr int L = kMass ? 3 : 1;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -782,24 +783,60 @@ __device__ Thresh radix_select(cg::cluster_group& cl, Ctx& c, const Src& src, un
   return Thresh{key, ti};
 }
 
-// k-th largest (k >= 1) of n keys in shared memory, rounded down to a multiple
-// of 2^(32 - 8*passes) (so it is <= the exact k-th largest); block-local.
-// Uses the first 256 words of hist as a count histogram.
-__device__ uint32_t local_kth_largest(Ctx& c, const uint32_t* keys, int n, uint32_t k, int passes) {
+// k-th largest (1 <= k <= n) of n keys in shared memory, rounded down to the resolution
+// the digit passes reach (so it is <= the exact k-th largest); block-local.  The bits
+// every key shares are found first (a block AND and OR), so the `passes` 8-bit digit
+// passes start right below them.  Digits are counted in eight private histograms (two
+// warps each) in `scratch` (2048 words), summed into the first 256 words of hist.
+__device__ __noinline__ uint32_t local_kth_largest(Ctx& c, const uint32_t* keys, int n, uint32_t k, int passes,
+                                                   uint32_t* scratch) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t* h = c.hist;
-  uint32_t prefix = 0, pmask = 0;
-  for (int d = 0; d < passes; ++d) {
-    const int shift = 24 - 8 * d;
-    for (int i = threadIdx.x; i < kBins; i += kThreads) h[i] = 0u;
+  // the shared leading bits
+  uint32_t a = 0xFFFFFFFFu, o = 0u;
+  for (int i = threadIdx.x; i < n; i += kThreads) {
+    a &= keys[i];
+    o |= keys[i];
+  }
+  a = __reduce_and_sync(kFull, a);
+  o = __reduce_or_sync(kFull, o);
+  if (lane == 0) c.red[warp] = (static_cast<unsigned long long>(a) << 32) | o;
+  __syncthreads();
+  a = 0xFFFFFFFFu;
+  o = 0u;
+#pragma unroll 1
+  for (int w = 0; w < kWarps; ++w) {
+    a &= static_cast<uint32_t>(c.red[w] >> 32);
+    o |= static_cast<uint32_t>(c.red[w]);
+  }
+  __syncthreads();
+  const uint32_t diff = a ^ o;
+  if (diff == 0u) return a;  // every key is the same
+  int top = 31 - __clz(diff);  // highest bit where keys differ
+  uint32_t prefix = top == 31 ? 0u : (a & (0xFFFFFFFFu << (top + 1)));
+  uint32_t pmask = top == 31 ? 0u : (0xFFFFFFFFu << (top + 1));
+#pragma unroll 1
+  for (int d = 0; d < passes && top >= 0; ++d) {
+    const int width = top + 1 < 8 ? top + 1 : 8;
+    const int shift = top + 1 - width;
+    const uint32_t dmask = (1u << width) - 1u;
+    for (int i = threadIdx.x; i < 8 * kBins; i += kThreads) scratch[i] = 0u;
     __syncthreads();
+    uint32_t* hp = scratch + (warp >> 1) * kBins;
     for (int base = 0; base < n; base += kThreads) {
       const int i = base + threadIdx.x;
       const uint32_t key = i < n ? keys[i] : 0u;
       const bool take = i < n && (key & pmask) == prefix;
-      const int bin = static_cast<int>((key >> shift) & 0xFFu);
+      const int bin = static_cast<int>((key >> shift) & dmask);
       const unsigned peers = __match_any_sync(kFull, take ? bin : -1);
-      if (take && lane == __ffs(peers) - 1) atomicAdd(&h[bin], static_cast<uint32_t>(__popc(peers)));
+      if (take && lane == __ffs(peers) - 1) atomicAdd(&hp[bin], static_cast<uint32_t>(__popc(peers)));
+    }
+    __syncthreads();
+    if (threadIdx.x < kBins) {
+      uint32_t t = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) t += scratch[j * kBins + threadIdx.x];
+      h[threadIdx.x] = t;
     }
     __syncthreads();
     if (warp == 0) {
@@ -837,8 +874,9 @@ __device__ uint32_t local_kth_largest(Ctx& c, const uint32_t* keys, int n, uint3
     }
     __syncthreads();
     prefix |= static_cast<uint32_t>(c.misc[0]) << shift;
-    pmask |= 0xFFu << shift;
+    pmask |= dmask << shift;
     k = static_cast<uint32_t>(c.misc[1]);
+    top = shift - 1;
     __syncthreads();
   }
   return prefix;
@@ -854,7 +892,7 @@ struct Boundary {
   unsigned long long tau;   // target used
 };
 template <int L>
-__device__ Boundary find_boundary(cg::cluster_group& cl, Ctx& c, const Bins<L>& h, unsigned long long* sup,
+__device__ __noinline__ Boundary find_boundary(cg::cluster_group& cl, Ctx& c, const Bins<L>& h, unsigned long long* sup,
                                   unsigned long long tau, bool p_mode, float p) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int CS = static_cast<int>(cl.num_blocks());
@@ -926,7 +964,7 @@ __device__ __forceinline__ void super_sums(const Bins<L>& h, unsigned long long*
 // excl < need <= excl + w (count mode: w = 1; mass mode: w = fixed mass).
 // Returns false (uniformly) if the lists do not fit.
 template <bool kMass>
-__device__ bool resolve_small(cg::cluster_group& cl, Ctx& c, unsigned long long need, Thresh* out) {
+__device__ __noinline__ bool resolve_small(cg::cluster_group& cl, Ctx& c, unsigned long long need, Thresh* out) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int CS = static_cast<int>(cl.num_blocks());
   unsigned long long* all = c.small + kSmall;
@@ -1065,6 +1103,14 @@ __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P)
   if (my_rows > 0) issue_load(row_at(0));
   uint32_t parity = 0;
 
+  // groups of 128 elements over the row (the last CTA's partial group included)
+  int G128 = 0;
+  for (int r = 0; r < CS; ++r) {
+    int nr = static_cast<int>(V - static_cast<int64_t>(r) * P.nc);
+    nr = nr < 0 ? 0 : (nr > P.nc ? P.nc : nr);
+    G128 += (((nr + 3) >> 2) + 31) >> 5;
+  }
+
   for (int ri = 0; ri < my_rows; ++ri, parity ^= 1u) {
     const int64_t row = row_at(ri);
     const int64_t next = ri + 1 < my_rows ? row_at(ri + 1) : -1;
@@ -1082,6 +1128,11 @@ __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P)
     const bool p_nan = isnan(p);
     const bool single = greedyT || (!p_nan && p <= 0.0f) || (topk_on && k == 1);
     const bool topp_on = !single && !p_nan && p > 0.0f && p < 1.0f;
+    // top-k bound: split the 128-element groups until there are at least k of them
+    // (while the gathered maxima still fit kGallCap)
+    int gsh = 0;
+    if (topk_on && !single)
+      while ((1 << gsh) < kGroupSplit && (G128 << gsh) < k && (G128 << (gsh + 1)) <= kGallCap) ++gsh;
 
     // prefetch up to four seen ids per thread while the chunk is in flight
     int32_t pid[4];
@@ -1193,10 +1244,14 @@ __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P)
           }
           if (changed) x4[g] = make_float4(vv[0], vv[1], vv[2], vv[3]);
         }
-        // the warp's 32 float4s are one group of 128 consecutive elements
-        gk = __reduce_max_sync(kFull, gk);
-        if (lane == 0 && base + 32 * warp < n4) c.gmax[(base >> 5) + warp] = gk;
+        // the warp's 32 float4s are 1 << gsh groups of 128 >> gsh consecutive elements
         tmax = gk > tmax ? gk : tmax;
+        for (int o = 16 >> gsh; o; o >>= 1) {
+          const uint32_t y = __shfl_xor_sync(kFull, gk, o);
+          gk = y > gk ? y : gk;
+        }
+        if ((lane & ((32 >> gsh) - 1)) == 0 && base + 32 * warp < n4)
+          c.gmax[(((base >> 5) + warp) << gsh) + (lane >> (5 - gsh))] = gk;
       }
     }
     {
@@ -1268,13 +1323,8 @@ __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P)
       th = Thresh{mkey, chosen};
     } else if (topk_on) {
       // ---- top-k: lower bound from the group maxima ------------------------------
-      const int ng_full = (P.nc + 127) / 128;
-      int G = 0;
-      for (int r = 0; r < CS; ++r) {
-        int nr = static_cast<int>(V - static_cast<int64_t>(r) * P.nc);
-        nr = nr < 0 ? 0 : (nr > P.nc ? P.nc : nr);
-        G += (((nr + 3) >> 2) + 31) >> 5;
-      }
+      const int ng_full = ((P.nc + 127) / 128) << gsh;
+      const int G = G128 << gsh;
       bool fast = G >= k && G <= kGallCap;
       if (fast) {
         uint32_t* gall = reinterpret_cast<uint32_t*>(c.hist) + kBins;  // after the 256 count words
@@ -1283,7 +1333,7 @@ __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P)
           gall[i] = *cl.map_shared_rank(c.gmax + j, r);
         }
         __syncthreads();
-        uint32_t gkey = local_kth_largest(c, gall, G, static_cast<uint32_t>(k), 3);
+        uint32_t gkey = local_kth_largest(c, gall, G, static_cast<uint32_t>(k), 2, c.fine);
         if (gkey < kKeyNegInf) gkey = kKeyNegInf;
         const float g = kfloat(gkey);  // <= the k-th largest raw group maximum
         const float t0 = __fdiv_rn(g, T);

@@ -1526,7 +1526,7 @@ __device__ __noinline__ uint32_t rp_pass_b(const RowCtx& rc, float H, int bstar,
 // atomics; the row kernel reads the record instead of running pass A, and zeroes it for
 // the next launch.
 constexpr size_t kPRecBytes = 32896;  // sums u64[2048], race words u64[2048], M, H, padding
-constexpr int kPreMaxChunks = 16;     // CTAs of the pre-pass per row, at most
+constexpr int kPreMaxChunks = 8;      // CTAs of the pre-pass per row, at most (measured: 8 beat 13-16 at B=256)
 
 struct PRec {
   unsigned long long* sums;  // per bin: the sum of w24 over the row
