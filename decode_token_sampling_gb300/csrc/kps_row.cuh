@@ -1675,23 +1675,45 @@ __device__ __noinline__ int32_t rwide_row(const RowCtx& rc, const RowSmem& sm, c
     constexpr int per = kRPBins / kRT;
     double m[per];
     double sum = 0.0;
+    // this thread's bins, every load of a source issued before any is used
+    const int b0 = per * static_cast<int>(threadIdx.x);
+    unsigned long long cb[per];
+    float fb[per];
 #pragma unroll
-    for (int e = 0; e < per; ++e) {
-      const int b = per * static_cast<int>(threadIdx.x) + e;
-      unsigned long long c = 0, wb = 0;
-      if (from_rec) {
-        c = __ldcg(rec->sums + b);
-        wb = __ldcg(rec->ub + b);
-      } else {
-        for (int r = 0; r < tm.C; ++r) {
-          const uint32_t* hr = tm.remote(sm.hist, r);
-          const unsigned long long x = tm.remote(sm.cw, r)[b];
-          c += static_cast<unsigned long long>(hr[b]) + (static_cast<unsigned long long>(hr[kRPBins + b]) << 12);
-          wb = x > wb ? x : wb;
+    for (int e = 0; e < per; ++e) fb[e] = kExpBin.v[b0 + e];
+    if (from_rec) {
+#pragma unroll
+      for (int e = 0; e < per; ++e) {
+        cb[e] = __ldcg(rec->sums + b0 + e);
+        ubest[e] = __ldcg(rec->ub + b0 + e);
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < per; ++e) {
+        cb[e] = 0ull;
+        ubest[e] = 0ull;
+      }
+      for (int r = 0; r < tm.C; ++r) {
+        const uint32_t* hr = tm.remote(sm.hist, r);
+        const unsigned long long* ur = tm.remote(sm.cw, r);
+        uint32_t lo[per], hi[per];
+        unsigned long long x[per];
+#pragma unroll
+        for (int e = 0; e < per; ++e) {
+          lo[e] = hr[b0 + e];
+          hi[e] = hr[kRPBins + b0 + e];
+          x[e] = ur[b0 + e];
+        }
+#pragma unroll
+        for (int e = 0; e < per; ++e) {
+          cb[e] += static_cast<unsigned long long>(lo[e]) + (static_cast<unsigned long long>(hi[e]) << 12);
+          ubest[e] = x[e] > ubest[e] ? x[e] : ubest[e];
         }
       }
-      ubest[e] = wb;
-      m[e] = static_cast<double>(c) * 5.9604644775390625e-8 * static_cast<double>(kExpBin.v[b]);
+    }
+#pragma unroll
+    for (int e = 0; e < per; ++e) {
+      m[e] = static_cast<double>(cb[e]) * 5.9604644775390625e-8 * static_cast<double>(fb[e]);
       sum += m[e];
     }
     if (threadIdx.x == 0) sm.misc[kMBin] = static_cast<unsigned long long>(kRPBins);
