@@ -777,23 +777,23 @@ __device__ __forceinline__ uint32_t rk_stream(const RowCtx& rc, float tau_raw, b
   const unsigned lt = (1u << lane) - 1u;
   const uint4* xr = rc.x;
   float* out = rc.out;
-  const int nv = rc.nv;
+  const int g1 = rc.g1;  // this CTA's part of the row: [rc.g0, g1)
   const uint32_t* bitmap = rc.bitmap;
   const bool pen_on = rc.pen_on;
   const float pen = rc.pen;
   const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
   uint32_t wcnt = 0;
-  for (int base = 0; base < nv; base += kRT * kRU) {
+  for (int base = rc.g0; base < g1; base += kRT * kRU) {
     uint4 w[kRU];
 #pragma unroll
     for (int u = 0; u < kRU; ++u) {
       const int g = base + u * kRT + static_cast<int>(threadIdx.x);
-      w[u] = g < nv ? ld_row16(xr + g, pol) : make_uint4(0u, 0u, 0u, 0u);
+      w[u] = g < g1 ? ld_row16(xr + g, pol) : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
     for (int u = 0; u < kRU; ++u) {
       const int g = base + u * kRT + static_cast<int>(threadIdx.x);
-      const bool in = g < nv;
+      const bool in = g < g1;
       if (out != nullptr && in) {
         float4* o = reinterpret_cast<float4*>(out) + g * (G / 4);
 #pragma unroll
@@ -1039,83 +1039,6 @@ struct RowSmem {
 constexpr Thresh kKeepAll{1u, -1};  // kept_by(any real key) holds; empty slots (key 0) fail
 
 // Top-k and one-element rows; returns the chosen index.
-template <bool kBF16>
-__device__ __noinline__ int32_t rk_row(const RowCtx& rc, const RowSmem& sm, uint32_t keff, bool single, bool topp_on,
-                                       float p, float eps, bool exact, bool sampled) {
-  uint32_t& s_cnt = *reinterpret_cast<uint32_t*>(sm.misc + kMCnt);
-  uint32_t* segcnt = reinterpret_cast<uint32_t*>(sm.misc + kMSeg);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const bool keep_all = rc.V <= kRKeepAllV && !exact;
-  uint32_t tau_key = 0u;
-  float tau_raw = -INFINITY;
-  if (exact) {
-    tau_raw = __int_as_float(0x7fffffff);  // nothing passes: the exact select below takes over
-  } else if (!keep_all) {
-    uint32_t* samp = reinterpret_cast<uint32_t*>(sm.wbuf);
-    if (!sampled) rsample_load<kBF16>(rc, samp);
-    // the streaming pass's first two rounds of loads, asked of L2 during the selection
-    for (int o = static_cast<int>(threadIdx.x) * 128; o < 2 * kRT * kRU * 16 && o < rc.nv * 16; o += kRT * 128)
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(rc.x) + o));
-    const int64_t want = (5 * static_cast<int64_t>(keff)) / 2 + 512;
-    int64_t r = (want * kRSamp + rc.V - 1) / rc.V + 1;
-    if (r > kRSamp) r = kRSamp;
-    tau_key = rsample_rank(samp, static_cast<uint32_t>(r), sm.hist, sm.red, sm.misc);
-    const float tv = kfloat(tau_key);
-    // a threshold at or below -inf would take the whole row: go to the exact select
-    tau_raw = (tau_key > kKeyNegInf && !isnan(tv)) ? raw_floor(tv, rc.T, rc.identity) : __int_as_float(0x7fffffff);
-  }
-  const uint32_t wc = rk_stream<kBF16>(rc, tau_raw, keep_all, sm.cw + warp * kRSeg, l2_policy_first());
-  if (lane == 0) segcnt[warp] = wc;
-  __syncthreads();
-  bool over = false;
-#pragma unroll
-  for (int w = 0; w < kRW; ++w) over |= segcnt[w] > static_cast<uint32_t>(kRSeg);
-  unsigned long long top;
-  uint32_t mn;
-  uint32_t n = rk_normalize(sm.cw, segcnt, tau_key, rc.div, rc.identity, sm.red, &top, &mn);
-  if (over || n < keff) {
-    // the sample missed: exact k-th element over the row, then collect the k kept
-    const Thresh th = rrow_select<kBF16, false>(rc, keff, 0.0f, sm.hist, sm.red, sm.misc);
-    for (int i = threadIdx.x; i < kRCap; i += kRT) sm.cw[i] = 0ull;
-    if (threadIdx.x == 0) s_cnt = 0u;
-    __syncthreads();
-    unsigned long long b0 = 0, b1 = 0;
-    rrow_pass<kBF16>(rc, l2_policy_normal(), [&](bool valid, float, uint32_t key, int idx) {
-      const bool keep = valid && kept_by(key, idx, th.key, th.idx);
-      const uint32_t pos = rwarp_reserve(keep ? 1u : 0u, s_cnt);
-      if (keep && pos < static_cast<uint32_t>(kRCap)) {
-        const unsigned long long w = order_word(key, idx);
-        sm.cw[pos] = w;
-        b0 = w > b0 ? w : b0;
-        const unsigned long long nk = static_cast<uint32_t>(~key);
-        b1 = nk > b1 ? nk : b1;
-      }
-    });
-    rblock_max2(b0, b1, sm.red);
-    top = b0;
-    mn = ~static_cast<uint32_t>(b1);
-    n = keff;  // exactly keff elements are kept by th
-  }
-  const uint32_t mx = static_cast<uint32_t>(top >> 32);
-  const float M = kfloat(mx);
-  if (single) {
-    const int32_t idx = static_cast<int32_t>(~static_cast<uint32_t>(top));
-    if (threadIdx.x == 0 && rc.out) rc.out[idx] = M;
-    return idx;
-  }
-  const Thresh tk = n > keff ? rbuf_kth(sm.cw, kRCap, keff, mx, mn, sm.hist, sm.wbuf, sm.red, sm.misc) : kKeepAll;
-  const int ns = rbuf_gather(sm.cw, kRCap, tk, sm.wbuf, kTopKMax, sm.red);  // the k survivors
-  Thresh th = kKeepAll;
-  if (topp_on && ns > 1) th = rk_topp(sm.wbuf, ns, M, p, sm.hist, sm.cw, sm.red, sm.misc);
-  unsigned long long rb = 0, first = 0;
-  rlist_race(sm.wbuf, ns, th, M, rc, eps, rb, first);
-  rblock_max2(rb, first, sm.red);
-  const unsigned long long c = rb ? rb : first;
-  return static_cast<int32_t>(~static_cast<uint32_t>(c));
-}
-
-// ---- rows shared by the CTAs of a cluster: top-p-only and keep-all rows -------------------
-
 // The CTAs that work on one row.  C == 1: this CTA alone (barriers are __syncthreads);
 // C > 1: the C CTAs of the thread-block cluster, each on its own part of the row,
 // exchanging partial results through distributed shared memory.
@@ -1159,6 +1082,109 @@ struct Team {
     return C > 1 ? cg::this_cluster().map_shared_rank(p, r) : p;
   }
 };
+
+template <bool kBF16>
+__device__ __noinline__ int32_t rk_row(const RowCtx& rc, const RowSmem& sm, const Team& tm, uint32_t keff, bool single,
+                                       bool topp_on, float p, float eps, bool exact, bool sampled) {
+  uint32_t& s_cnt = *reinterpret_cast<uint32_t*>(sm.misc + kMCnt);
+  uint32_t* segcnt = reinterpret_cast<uint32_t*>(sm.misc + kMSeg);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool keep_all = rc.V <= kRKeepAllV && !exact;
+  RowCtx whole = rc;  // the whole row (rc is this CTA's part when a team shares the row)
+  whole.g0 = 0;
+  whole.g1 = rc.nv;
+  uint32_t tau_key = 0u;
+  float tau_raw = -INFINITY;
+  if (exact) {
+    tau_raw = __int_as_float(0x7fffffff);  // nothing passes: the exact select below takes over
+  } else if (!keep_all) {
+    uint32_t* samp = reinterpret_cast<uint32_t*>(sm.wbuf);
+    if (!sampled) rsample_load<kBF16>(rc, samp);
+    // the streaming pass's first two rounds of loads, asked of L2 during the selection
+    for (int o = static_cast<int>(threadIdx.x) * 128; o < 2 * kRT * kRU * 16 && o < (rc.g1 - rc.g0) * 16; o += kRT * 128)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(rc.x + rc.g0) + o));
+    const int64_t want = (5 * static_cast<int64_t>(keff)) / 2 + 512;
+    int64_t r = (want * kRSamp + rc.V - 1) / rc.V + 1;
+    if (r > kRSamp) r = kRSamp;
+    tau_key = rsample_rank(samp, static_cast<uint32_t>(r), sm.hist, sm.red, sm.misc);
+    const float tv = kfloat(tau_key);
+    // a threshold at or below -inf would take the whole row: go to the exact select
+    tau_raw = (tau_key > kKeyNegInf && !isnan(tv)) ? raw_floor(tv, rc.T, rc.identity) : __int_as_float(0x7fffffff);
+  }
+  const uint32_t wc = rk_stream<kBF16>(rc, tau_raw, keep_all, sm.cw + warp * kRSeg, l2_policy_first());
+  if (lane == 0) segcnt[warp] = wc;
+  __syncthreads();
+  if (tm.C > 1) {
+    // a team streamed the parts of one row against the same threshold (every member
+    // samples the same elements): rank 0 appends the others' warp segments behind its own
+    // (a segment that would overflow marks the buffer overflowed), then goes on alone
+    tm.sync();
+    if (tm.rank == 0) {
+      uint32_t own = segcnt[warp];
+      for (int r = 1; r < tm.C; ++r) {
+        const uint32_t other = *tm.remote(segcnt + warp, r);
+        const unsigned long long* src = tm.remote(sm.cw + warp * kRSeg, r);
+        const bool fits = own <= static_cast<uint32_t>(kRSeg) && other <= static_cast<uint32_t>(kRSeg) &&
+                          own + other <= static_cast<uint32_t>(kRSeg);
+        if (fits)
+          for (uint32_t i = lane; i < other; i += 32) sm.cw[warp * kRSeg + own + i] = src[i];
+        own = fits ? own + other : static_cast<uint32_t>(kRSeg) + 1u;
+      }
+      __syncwarp();
+      if (lane == 0) segcnt[warp] = own;
+    }
+    tm.sync();  // the other members' segments are read; they leave the row
+    if (tm.rank != 0) return -1;
+  }
+  bool over = false;
+#pragma unroll
+  for (int w = 0; w < kRW; ++w) over |= segcnt[w] > static_cast<uint32_t>(kRSeg);
+  unsigned long long top;
+  uint32_t mn;
+  uint32_t n = rk_normalize(sm.cw, segcnt, tau_key, rc.div, rc.identity, sm.red, &top, &mn);
+  if (over || n < keff) {
+    // the sample missed: exact k-th element over the row, then collect the k kept
+    const Thresh th = rrow_select<kBF16, false>(whole, keff, 0.0f, sm.hist, sm.red, sm.misc);
+    for (int i = threadIdx.x; i < kRCap; i += kRT) sm.cw[i] = 0ull;
+    if (threadIdx.x == 0) s_cnt = 0u;
+    __syncthreads();
+    unsigned long long b0 = 0, b1 = 0;
+    rrow_pass<kBF16>(whole, l2_policy_normal(), [&](bool valid, float, uint32_t key, int idx) {
+      const bool keep = valid && kept_by(key, idx, th.key, th.idx);
+      const uint32_t pos = rwarp_reserve(keep ? 1u : 0u, s_cnt);
+      if (keep && pos < static_cast<uint32_t>(kRCap)) {
+        const unsigned long long w = order_word(key, idx);
+        sm.cw[pos] = w;
+        b0 = w > b0 ? w : b0;
+        const unsigned long long nk = static_cast<uint32_t>(~key);
+        b1 = nk > b1 ? nk : b1;
+      }
+    });
+    rblock_max2(b0, b1, sm.red);
+    top = b0;
+    mn = ~static_cast<uint32_t>(b1);
+    n = keff;  // exactly keff elements are kept by th
+  }
+  const uint32_t mx = static_cast<uint32_t>(top >> 32);
+  const float M = kfloat(mx);
+  if (single) {
+    const int32_t idx = static_cast<int32_t>(~static_cast<uint32_t>(top));
+    if (threadIdx.x == 0 && rc.out) rc.out[idx] = M;
+    return idx;
+  }
+  const Thresh tk = n > keff ? rbuf_kth(sm.cw, kRCap, keff, mx, mn, sm.hist, sm.wbuf, sm.red, sm.misc) : kKeepAll;
+  const int ns = rbuf_gather(sm.cw, kRCap, tk, sm.wbuf, kTopKMax, sm.red);  // the k survivors
+  Thresh th = kKeepAll;
+  if (topp_on && ns > 1) th = rk_topp(sm.wbuf, ns, M, p, sm.hist, sm.cw, sm.red, sm.misc);
+  unsigned long long rb = 0, first = 0;
+  rlist_race(sm.wbuf, ns, th, M, rc, eps, rb, first);
+  rblock_max2(rb, first, sm.red);
+  const unsigned long long c = rb ? rb : first;
+  return static_cast<int32_t>(~static_cast<uint32_t>(c));
+}
+
+// ---- rows shared by the CTAs of a cluster: top-p-only and keep-all rows -------------------
+
 
 // The largest penalised raw value of this CTA's part of the row, as a key.
 template <bool kBF16>
@@ -2057,7 +2083,7 @@ __device__ int rbuild_items(const Params& P, int C, int rank, int cluster, int n
       } else {
         const int64_t ko = static_cast<int64_t>(ex & 0xFFFFFull);
         unit = (wide_last ? 0 : nwide) + ko / per;
-        slot = ko % per;
+        slot = (per == 1 && P.V > kRKeepAllV) ? rank : ko % per;  // one row per unit: the CTAs share it
       }
       if (unit % nclusters == cluster && slot == rank) {
         items[unit / nclusters] = wide ? static_cast<int32_t>(-(r + 2)) : static_cast<int32_t>(r);
@@ -2104,7 +2130,7 @@ __device__ int rbuild_items(const Params& P, int C, int rank, int cluster, int n
       } else {
         const int64_t ko = static_cast<int64_t>(kbase + (ex & 0xFFFFFFFFull));
         unit = (wide_last ? 0 : static_cast<int64_t>(nwide)) + ko / per;
-        slot = ko % per;
+        slot = (per == 1 && P.V > kRKeepAllV) ? rank : ko % per;  // one row per unit: the CTAs share it
       }
       if (unit % nclusters == cluster && slot == rank) {
         items[unit / nclusters] = wide ? static_cast<int32_t>(-(r + 2)) : static_cast<int32_t>(r);
@@ -2345,13 +2371,16 @@ __global__ void __launch_bounds__(kRT, 2) kps_row_kernel(const Params P) {
       row = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(it) * gridDim.x;
       wide = row_is_wide(P, row);
     }
-    const Team& tm = wide ? team : alone;
+    // with every row in a cluster of its own, a top-k row (longer than the rows taken whole)
+    // is shared by the cluster's CTAs, each streaming its part against the same threshold
+    const bool kteam = !wide && shared_rows && P.B <= nclusters && P.V > kRKeepAllV;
+    const Team& tm = (wide || kteam) ? team : alone;
     RowCtx rc;
     const bool sample = !wide && !P.exact && P.V > kRKeepAllV;
     const RowFlags f = row_setup<kBF16>(P, row, sm, tm.rank, tm.C, &rc, sample);
     int32_t chosen;
     if (!wide) {
-      chosen = rk_row<kBF16>(rc, sm, f.single ? 1u : static_cast<uint32_t>(f.k), f.single, f.topp_on, f.p, P.eps,
+      chosen = rk_row<kBF16>(rc, sm, tm, f.single ? 1u : static_cast<uint32_t>(f.k), f.single, f.topp_on, f.p, P.eps,
                              P.exact != 0, sample);
     } else {
       PRec rec;
