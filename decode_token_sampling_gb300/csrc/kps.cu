@@ -81,6 +81,7 @@ constexpr int kCapLoc = 1024;       // candidates one CTA may hold
 constexpr int kGallCap = 2048;      // group maxima one row may have for the top-k bound
 constexpr int kGroupSplit = 8;      // groups of 128 elements split up to 8 ways (16 elements)
 constexpr int kLinBins = 2048;      // linear count bins of the top-k candidate pass
+static_assert(kLinBins == 1 << 11, "the k-th bound keeps 11 bits of the key span");
 constexpr int kLinBinsP = 1024;     // linear mass bins (width 1/16 of d = max - x) of top-p-only rows
 constexpr int kFineBins = 1024;     // linear bins of the refinement histogram (top-p-only rows)
 constexpr int kSmall = 64;          // boundary-bin elements resolved by exact ranking
@@ -783,103 +784,61 @@ __device__ __noinline__ Thresh radix_select(cg::cluster_group& cl, Ctx& c, const
   return Thresh{key, ti};
 }
 
-// k-th largest (1 <= k <= n) of n keys in shared memory, rounded down to the resolution
-// the digit passes reach (so it is <= the exact k-th largest); block-local.  The bits
-// every key shares are found first (a block AND and OR), so the `passes` 8-bit digit
-// passes start right below them.  Digits are counted in eight private histograms (two
-// warps each) in `scratch` (2048 words), summed into the first 256 words of hist.
-__device__ __noinline__ uint32_t local_kth_largest(Ctx& c, const uint32_t* keys, int n, uint32_t k, int passes,
-                                                   uint32_t* scratch) {
+// A lower bound on the k-th largest (1 <= k <= n) of n keys in shared memory: the lower
+// edge of the bin that holds the k-th largest, the bins being the keys' offsets from the
+// smallest key shifted right until at most kLinBins remain (one counting pass; the bound
+// is at most one bin below the exact value).  Block-local; `h` is kLinBins words of
+// scratch.
+__device__ __noinline__ uint32_t local_kth_lower(Ctx& c, const uint32_t* keys, int n, uint32_t k, uint32_t* h) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t* h = c.hist;
-  // the shared leading bits
-  uint32_t a = 0xFFFFFFFFu, o = 0u;
+  uint32_t mx = 0u, mn = 0xFFFFFFFFu;
   for (int i = threadIdx.x; i < n; i += kThreads) {
-    a &= keys[i];
-    o |= keys[i];
+    const uint32_t key = keys[i];
+    mx = key > mx ? key : mx;
+    mn = key < mn ? key : mn;
   }
-  a = __reduce_and_sync(kFull, a);
-  o = __reduce_or_sync(kFull, o);
-  if (lane == 0) c.red[warp] = (static_cast<unsigned long long>(a) << 32) | o;
+  mx = __reduce_max_sync(kFull, mx);
+  mn = __reduce_min_sync(kFull, mn);
+  if (lane == 0) c.red[warp] = (static_cast<unsigned long long>(mx) << 32) | mn;
+  for (int i = threadIdx.x; i < kLinBins; i += kThreads) h[i] = 0u;
   __syncthreads();
-  a = 0xFFFFFFFFu;
-  o = 0u;
-#pragma unroll 1
-  for (int w = 0; w < kWarps; ++w) {
-    a &= static_cast<uint32_t>(c.red[w] >> 32);
-    o |= static_cast<uint32_t>(c.red[w]);
+  {
+    const unsigned long long v = c.red[lane & (kWarps - 1)];
+    mx = __reduce_max_sync(kFull, static_cast<uint32_t>(v >> 32));
+    mn = __reduce_min_sync(kFull, static_cast<uint32_t>(v));
+  }
+  __syncthreads();  // c.red is reused by the scan below
+  const uint32_t span = mx - mn;
+  if (span == 0u) return mn;
+  // kLinBins = 2^11: keep the top 11 bits of the span
+  const int used = 32 - __clz(span);
+  const int shift = used > 11 ? used - 11 : 0;
+  for (int i = threadIdx.x; i < n; i += kThreads) atomicAdd(&h[(keys[i] - mn) >> shift], 1u);
+  __syncthreads();
+  // thread t owns bins kLinBins-1-4t ... kLinBins-4-4t (largest first)
+  constexpr int per = kLinBins / kThreads;
+  uint32_t cnt[per];
+  uint32_t sum = 0;
+#pragma unroll
+  for (int e = 0; e < per; ++e) {
+    cnt[e] = h[kLinBins - 1 - (per * static_cast<int>(threadIdx.x) + e)];
+    sum += cnt[e];
+  }
+  uint32_t tot;
+  const uint32_t ex = block_excl_scan_u32(sum, &tot, c.red);
+  if (ex < k && ex + sum >= k) {
+    uint32_t acc = ex;
+#pragma unroll
+    for (int e = 0; e < per; ++e) {
+      if (acc < k && acc + cnt[e] >= k)
+        c.misc[0] = static_cast<unsigned long long>(kLinBins - 1 - (per * static_cast<int>(threadIdx.x) + e));
+      acc += cnt[e];
+    }
   }
   __syncthreads();
-  const uint32_t diff = a ^ o;
-  if (diff == 0u) return a;  // every key is the same
-  int top = 31 - __clz(diff);  // highest bit where keys differ
-  uint32_t prefix = top == 31 ? 0u : (a & (0xFFFFFFFFu << (top + 1)));
-  uint32_t pmask = top == 31 ? 0u : (0xFFFFFFFFu << (top + 1));
-#pragma unroll 1
-  for (int d = 0; d < passes && top >= 0; ++d) {
-    const int width = top + 1 < 8 ? top + 1 : 8;
-    const int shift = top + 1 - width;
-    const uint32_t dmask = (1u << width) - 1u;
-    for (int i = threadIdx.x; i < 8 * kBins; i += kThreads) scratch[i] = 0u;
-    __syncthreads();
-    uint32_t* hp = scratch + (warp >> 1) * kBins;
-    for (int base = 0; base < n; base += kThreads) {
-      const int i = base + threadIdx.x;
-      const uint32_t key = i < n ? keys[i] : 0u;
-      const bool take = i < n && (key & pmask) == prefix;
-      const int bin = static_cast<int>((key >> shift) & dmask);
-      const unsigned peers = __match_any_sync(kFull, take ? bin : -1);
-      if (take && lane == __ffs(peers) - 1) atomicAdd(&hp[bin], static_cast<uint32_t>(__popc(peers)));
-    }
-    __syncthreads();
-    if (threadIdx.x < kBins) {
-      uint32_t t = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) t += scratch[j * kBins + threadIdx.x];
-      h[threadIdx.x] = t;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      // lane l owns bins 255 - 8l ... 248 - 8l (largest first)
-      uint32_t b[8];
-      uint32_t sum = 0;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        b[e] = h[255 - 8 * lane - e];
-        sum += b[e];
-      }
-      const uint32_t inc = warp_incl_scan_u32(sum, lane);
-      const unsigned m = __ballot_sync(kFull, inc >= k);
-      if (m) {
-        const int L = __ffs(m) - 1;
-        if (lane == L) {
-          uint32_t acc = inc - sum;
-          int beta = 255 - 8 * lane;
-          uint32_t newk = k - acc;
-          for (int e = 0; e < 8; ++e) {
-            if (acc + b[e] >= k) {
-              beta = 255 - 8 * lane - e;
-              newk = k - acc;
-              break;
-            }
-            acc += b[e];
-          }
-          c.misc[0] = static_cast<unsigned long long>(beta);
-          c.misc[1] = newk;
-        }
-      } else if (lane == 0) {
-        c.misc[0] = 0ull;  // cannot happen for k <= n
-        c.misc[1] = 1ull;
-      }
-    }
-    __syncthreads();
-    prefix |= static_cast<uint32_t>(c.misc[0]) << shift;
-    pmask |= dmask << shift;
-    k = static_cast<uint32_t>(c.misc[1]);
-    top = shift - 1;
-    __syncthreads();
-  }
-  return prefix;
+  const uint32_t beta = static_cast<uint32_t>(c.misc[0]);
+  __syncthreads();
+  return mn + (beta << shift);  // the smallest key of bin beta
 }
 
 // After cl.sync: scans the cluster-wide histogram (nb bins in `h`, super sums
@@ -1246,9 +1205,13 @@ __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P)
         }
         // the warp's 32 float4s are 1 << gsh groups of 128 >> gsh consecutive elements
         tmax = gk > tmax ? gk : tmax;
-        for (int o = 16 >> gsh; o; o >>= 1) {
-          const uint32_t y = __shfl_xor_sync(kFull, gk, o);
-          gk = y > gk ? y : gk;
+        if (gsh == 0) {
+          gk = __reduce_max_sync(kFull, gk);
+        } else {
+          for (int o = 16 >> gsh; o; o >>= 1) {
+            const uint32_t y = __shfl_xor_sync(kFull, gk, o);
+            gk = y > gk ? y : gk;
+          }
         }
         if ((lane & ((32 >> gsh) - 1)) == 0 && base + 32 * warp < n4)
           c.gmax[(((base >> 5) + warp) << gsh) + (lane >> (5 - gsh))] = gk;
@@ -1333,7 +1296,7 @@ __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P)
           gall[i] = *cl.map_shared_rank(c.gmax + j, r);
         }
         __syncthreads();
-        uint32_t gkey = local_kth_largest(c, gall, G, static_cast<uint32_t>(k), 2, c.fine);
+        uint32_t gkey = local_kth_lower(c, gall, G, static_cast<uint32_t>(k), c.fine);
         if (gkey < kKeyNegInf) gkey = kKeyNegInf;
         const float g = kfloat(gkey);  // <= the k-th largest raw group maximum
         const float t0 = __fdiv_rn(g, T);
