@@ -689,11 +689,7 @@ __device__ __noinline__ Thresh radix_select(cg::cluster_group& cl, Ctx& c, const
         unsigned long long total = sv;
 #pragma unroll
         for (int o = 16; o; o >>= 1) total += __shfl_xor_sync(kFull, total, o);
-        const double t = ceil(static_cast<double>(p) * static_cast<double>(total));
-        unsigned long long tt = static_cast<unsigned long long>(t);
-        if (tt < 1ull) tt = 1ull;
-        if (tt > total) tt = total;
-        tau = tt;
+        tau = ceil_mul_p(p, total);
       }
       const unsigned long long inc = warp_incl_scan_u64(sv, lane);
       const unsigned m = __ballot_sync(kFull, lane < kSuper && inc >= tau);
@@ -863,11 +859,7 @@ __device__ __noinline__ Boundary find_boundary(cg::cluster_group& cl, Ctx& c, co
     const unsigned long long inc = warp_incl_scan_u64(s0 + s1, lane);
     if (p_mode) {
       const unsigned long long total = __shfl_sync(kFull, inc, 31);
-      const double t = ceil(static_cast<double>(p) * static_cast<double>(total));
-      unsigned long long tt = static_cast<unsigned long long>(t);
-      if (tt < 1ull) tt = 1ull;
-      if (tt > total) tt = total;
-      tau = tt;
+      tau = ceil_mul_p(p, total);
     }
     const unsigned m = __ballot_sync(kFull, inc >= tau && tau > 0);
     int beta = -1;

@@ -45,6 +45,45 @@ KPS_HD unsigned long long fixed_mass_of(float w) {
   return q + ((rem > half || (rem == half && (q & 1ull))) ? 1ull : 0ull);
 }
 
+// The high 64 bits of a * b.
+KPS_HD unsigned long long mul_hi_u64(unsigned long long a, unsigned long long b) {
+#if defined(__CUDA_ARCH__)
+  return __umul64hi(a, b);
+#else
+  return static_cast<unsigned long long>((static_cast<unsigned __int128>(a) * b) >> 64);
+#endif
+}
+
+// ceil(p * total) for 0 < p < 1 (a finite float), exactly: p's significand times total in
+// 128 bits, shifted right with the bits shifted out rounding up; clamped to [1, total].
+// (The top-p target of a fixed-point total mass, without FP64: a float -> 64-bit integer
+// conversion and double arithmetic run on the slow FP64 pipe of this GPU.)
+KPS_HD unsigned long long ceil_mul_p(float p, unsigned long long total) {
+  if (total == 0ull) return 0ull;
+  const uint32_t u = fixed_bits(p);
+  const int e = static_cast<int>((u >> 23) & 0xFFu);
+  if (e >= 127) return total;  // p >= 1 (or not finite): everything
+  const unsigned long long m = e ? ((u & 0x7FFFFFu) | 0x800000u) : (u & 0x7FFFFFu);  // p = m * 2^-s
+  const int s = e ? 150 - e : 149;  // >= 24 for p < 1
+  const unsigned long long lo = m * total, hi = mul_hi_u64(m, total);
+  unsigned long long t;
+  if (s >= 128) {
+    t = (lo | hi) ? 1ull : 0ull;
+  } else if (s >= 64) {
+    const int r = s - 64;
+    const unsigned long long q = r ? (hi >> r) : hi;
+    const bool rem = lo != 0ull || (r && (hi & ((1ull << r) - 1ull)) != 0ull);
+    t = q + (rem ? 1ull : 0ull);
+  } else {
+    const unsigned long long q = (lo >> s) | (hi << (64 - s));
+    const bool rem = (lo & ((1ull << s) - 1ull)) != 0ull;
+    t = q + (rem ? 1ull : 0ull);
+  }
+  if (t < 1ull) t = 1ull;
+  if (t > total) t = total;
+  return t;
+}
+
 }  // namespace kps
 
 #endif  // KPS_FIXED_H_

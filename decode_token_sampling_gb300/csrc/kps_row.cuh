@@ -866,11 +866,7 @@ __device__ __noinline__ uint32_t rk_normalize(unsigned long long* cw, const uint
 
 // Top-p target: ceil(p * S) clamped to [1, S].
 __device__ __forceinline__ unsigned long long rtopp_target(float p, unsigned long long S) {
-  const double t = ceil(static_cast<double>(p) * static_cast<double>(S));
-  unsigned long long tq = static_cast<unsigned long long>(t);
-  if (tq < 1ull) tq = 1ull;
-  if (tq > S) tq = S;
-  return tq;
+  return ceil_mul_p(p, S);
 }
 
 // Cut of a list sorted in descending order (kl[0..n), n <= kRSortMax): the number of
