@@ -719,19 +719,43 @@ __device__ __forceinline__ void rsample_load(const RowCtx& rc, uint32_t* samp) {
   rsample_finish(rc, sl, samp);
 }
 
-// The r-th largest sample key, rounded down to a multiple of 2^10 (two 11-bit digit
-// rounds): at least r samples are >= it.
+// The r-th largest sample key, rounded down: at least r samples are >= it.  The digit
+// rounds start below the bits every sample key shares (found from the smallest and largest
+// key), so that the keys spread over the 2048 bins of the first round instead of meeting
+// in a few (shared-memory adds to one word serialise); two 11-bit rounds of the offsets
+// from the smallest key.
 __device__ __noinline__ uint32_t rsample_rank(const uint32_t* samp, uint32_t r, uint32_t* h, unsigned long long* red,
                                               unsigned long long* misc) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t mx = 0u, mn = 0xFFFFFFFFu;
+  for (int i = threadIdx.x; i < kRSamp; i += kRT) {
+    mx = samp[i] > mx ? samp[i] : mx;
+    mn = samp[i] < mn ? samp[i] : mn;
+  }
+  mx = __reduce_max_sync(kFull, mx);
+  mn = __reduce_min_sync(kFull, mn);
+  if (lane == 0) red[warp] = (static_cast<unsigned long long>(mx) << 32) | mn;
+  __syncthreads();
+  {
+    const unsigned long long v = red[lane & (kRW - 1)];
+    mx = __reduce_max_sync(kFull, static_cast<uint32_t>(v >> 32));
+    mn = __reduce_min_sync(kFull, static_cast<uint32_t>(v));
+  }
+  __syncthreads();  // red is reused by the scans below
+  const uint32_t span = mx - mn;
+  if (span == 0u) return mn;
+  int top = 32 - __clz(span);  // offsets have this many bits
   uint32_t prefix = 0, pmask = 0, need = r;
   constexpr int per = 2048 / kRT;
-  for (int d = 0; d < 2; ++d) {
-    const int shift = d == 0 ? 21 : 10;
+  for (int d = 0; d < 2 && top > 0; ++d) {
+    const int width = top < 11 ? top : 11;
+    const int shift = top - width;
+    const uint32_t dmask = (1u << width) - 1u;
     for (int i = threadIdx.x; i < 2048; i += kRT) h[i] = 0u;
     __syncthreads();
     for (int i = threadIdx.x; i < kRSamp; i += kRT) {
-      const uint32_t key = samp[i];
-      if ((key & pmask) == prefix) sh_red_add(&h[(key >> shift) & 2047u], 1u);
+      const uint32_t o = samp[i] - mn;
+      if ((o & pmask) == prefix) sh_red_add(&h[(o >> shift) & dmask], 1u);
     }
     __syncthreads();
     uint32_t c[per];
@@ -756,11 +780,12 @@ __device__ __noinline__ uint32_t rsample_rank(const uint32_t* samp, uint32_t r, 
     }
     __syncthreads();
     prefix |= static_cast<uint32_t>(misc[kMSel0]) << shift;
-    pmask |= 2047u << shift;
+    pmask |= dmask << shift;
     need = static_cast<uint32_t>(misc[kMSel1]);
+    top = shift;
     __syncthreads();
   }
-  return prefix;
+  return mn + prefix;
 }
 
 // ---- top-k rows ----------------------------------------------------------------------------
