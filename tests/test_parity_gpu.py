@@ -545,3 +545,24 @@ def test_cluster_size_follows_the_batch():
             want = kps.query_launch(B, V, torch.bfloat16)["cluster_size"]
             assert kps.last_cluster_size() == want, (V, B, kps.last_cluster_size(), want)
     assert kps.query_launch(1, 65536, torch.bfloat16)["cluster_size"] > kps.query_launch(40, 65536, torch.bfloat16)["cluster_size"]
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("case", ["plain", "ties", "big_k", "no_logits"])
+def test_shared_topk_rows(dtype, case):
+    """Batches with at most one row per cluster of the row kernel: both CTAs of a cluster
+    stream one top-k row against the same sampled threshold and rank 0 merges their
+    candidate segments (a merge that would overflow a segment sends the row to the exact
+    whole-row select: the tied case).  Against the oracle, with filtered logits."""
+    import decode_token_sampling_gb300 as kps
+    kw = dict(plain=dict(k_range=(1, 1024)), ties=dict(ties=True, k_range=(500, 1024)),
+              big_k=dict(k_range=(1000, 1024), p_range=(0.9, 1.0)), no_logits=dict(need_logits=False))[case]
+    inp = make_random(100, 50000, seed=61 + len(case), dtype=dtype, penalty=1.2, n_seen=300, **kw)
+    ref = oracle.sample(inp)
+    kps.set_kernel_policy(kps.KERNEL_ROW)
+    try:
+        gi, gf = run_gpu(inp)
+        assert kps.last_kernel() == "kps_row_kernel"
+        assert kps.last_cluster_size() == 2
+    finally:
+        kps.set_kernel_policy(kps.KERNEL_AUTO)
+    compare(inp, ref, gi, gf, f"shared top-k rows {case} {dtype}")
