@@ -358,20 +358,29 @@ __device__ void rbitonic_desc(unsigned long long* a, int N) {
 // rest; returns their count.  Each thread reads a run of entries that other threads
 // wrote, so it starts with a barrier of its own.
 __device__ __noinline__ int rcompact_nonzero(unsigned long long* a, unsigned long long* red) {
-  constexpr int per = kRCap / kRT;
+  // warp w reads its kRSeg entries striped over its lanes (entry w * kRSeg + 32 e + lane):
+  // conflict-free shared loads, and (e, lane) order is the entries' order
+  constexpr int per = kRSeg / 32;
+  static_assert(per * 32 == kRSeg && kRSeg * kRW == kRCap, "striped segments");
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned lt = (1u << lane) - 1u;
   unsigned long long v[per];
-  uint32_t c = 0;
+  unsigned m[per];
+  uint32_t wtot = 0;
   __syncthreads();
 #pragma unroll
   for (int e = 0; e < per; ++e) {
-    v[e] = a[per * threadIdx.x + e];
-    c += v[e] != 0ull ? 1u : 0u;
+    v[e] = a[warp * kRSeg + e * 32 + lane];
+    m[e] = __ballot_sync(kFull, v[e] != 0ull);
+    wtot += __popc(m[e]);
   }
   uint32_t tot;
-  uint32_t pos = block_excl_scan_u32(c, &tot, red);
+  uint32_t pos = __shfl_sync(kFull, block_excl_scan_u32(lane == 0 ? wtot : 0u, &tot, red), 0);
 #pragma unroll
-  for (int e = 0; e < per; ++e)
-    if (v[e] != 0ull) a[pos++] = v[e];
+  for (int e = 0; e < per; ++e) {
+    if (v[e] != 0ull) a[pos + __popc(m[e] & lt)] = v[e];
+    pos += __popc(m[e]);
+  }
   __syncthreads();
   for (int i = static_cast<int>(tot) + static_cast<int>(threadIdx.x); i < kRCap; i += kRT) a[i] = 0ull;
   __syncthreads();
@@ -653,26 +662,33 @@ __device__ __noinline__ Thresh rbuf_kth(const unsigned long long* cw, int n, uin
 // counter would serialise one atomic per warp and round).
 __device__ __forceinline__ int rbuf_gather(const unsigned long long* cw, int n, Thresh th, unsigned long long* out,
                                            int cap, unsigned long long* red) {
-  constexpr int per = kRCap / kRT;
+  // warp w reads entries w * kRSeg + 32 e + lane (conflict-free; (e, lane) order is the
+  // buffer order)
+  constexpr int per = kRSeg / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned lt = (1u << lane) - 1u;
   unsigned long long w[per];
-  uint32_t c = 0;
+  unsigned m[per];
+  uint32_t wtot = 0;
 #pragma unroll
   for (int e = 0; e < per; ++e) {
-    const int i = per * static_cast<int>(threadIdx.x) + e;
+    const int i = warp * kRSeg + e * 32 + lane;
     w[e] = i < n ? cw[i] : 0ull;
     const bool keep = w[e] != 0ull && kept_by(static_cast<uint32_t>(w[e] >> 32),
                                               static_cast<int32_t>(~static_cast<uint32_t>(w[e])), th.key, th.idx);
     w[e] = keep ? w[e] : 0ull;
-    c += keep ? 1u : 0u;
+    m[e] = __ballot_sync(kFull, keep);
+    wtot += __popc(m[e]);
   }
   uint32_t tot;
-  uint32_t pos = block_excl_scan_u32(c, &tot, red);
+  uint32_t pos = __shfl_sync(kFull, block_excl_scan_u32(lane == 0 ? wtot : 0u, &tot, red), 0);
 #pragma unroll
   for (int e = 0; e < per; ++e) {
     if (w[e] != 0ull) {
-      if (pos < static_cast<uint32_t>(cap)) out[pos] = w[e];
-      ++pos;
+      const uint32_t q = pos + __popc(m[e] & lt);
+      if (q < static_cast<uint32_t>(cap)) out[q] = w[e];
     }
+    pos += __popc(m[e]);
   }
   __syncthreads();
   return static_cast<int>(tot) < cap ? static_cast<int>(tot) : cap;
