@@ -186,7 +186,9 @@ typedef struct {
                                 both compute the same results):
                                 0 = automatic (kps_sample and kps_sample_seeded
                                     always use it): the row kernel — one CTA per
-                                    row, the row read from global memory with
+                                    row (both CTAs of a 2-CTA cluster per row when
+                                    the batch gives every row a cluster of its
+                                    own), the row read from global memory with
                                     16-byte loads, two CTAs per SM — for batches
                                     of at least 64 rows whose rows are 16-byte
                                     aligned and V <= 262144; the cluster kernel —
