@@ -60,5 +60,15 @@ def build_spin_test(force: bool = False) -> str:
     return build(force=force, extra_flags=[f"-DKPS_TEST_SPIN_CYCLES={SPIN_TEST_CYCLES}LL"], out=SPIN_TEST_LIB)
 
 
+# Debug variant: every kernel's dynamic shared memory starts as a NaN pattern
+# (KPS_DEBUG_SENTINEL), so a read of shared memory that nothing in the launch wrote shows
+# up as a wrong result.
+SENTINEL_LIB = os.path.join(PKG, "libkps_sentinel.so")
+
+
+def build_sentinel(force: bool = False) -> str:
+    return build(force=force, extra_flags=["-DKPS_DEBUG_SENTINEL"], out=SENTINEL_LIB)
+
+
 if __name__ == "__main__":
     print(build(force=True, verbose=True))

@@ -965,6 +965,28 @@ __device__ __noinline__ bool resolve_small(cg::cluster_group& cl, Ctx& c, unsign
   return ok;
 }
 
+// Debug build (-DKPS_DEBUG_SENTINEL): every word of the block's dynamic shared memory
+// starts as a NaN pattern, so a word read before any thread of the launch wrote it shows
+// up as a wrong result instead of a previous launch's leftovers.  A barrier follows (a
+// cluster barrier when the launch has clusters, so that no member pushes into a CTA that
+// is still filling).  In other builds this is nothing.
+__device__ __forceinline__ void debug_fill_smem(unsigned char* base, bool cluster) {
+#ifdef KPS_DEBUG_SENTINEL
+  uint32_t nbytes;
+  asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(nbytes));
+  uint32_t* w = reinterpret_cast<uint32_t*>(base);
+  for (uint32_t i = threadIdx.x; i < nbytes / 4; i += blockDim.x) w[i] = 0x7FBADBADu;
+  if (cluster) {
+    cg::this_cluster().sync();
+  } else {
+    __syncthreads();
+  }
+#else
+  (void)base;
+  (void)cluster;
+#endif
+}
+
 // ------------------------------------------------------------------------------------------
 // The kernel: a persistent grid of clusters, one row per cluster at a time.
 // ------------------------------------------------------------------------------------------
@@ -972,6 +994,7 @@ template <bool kBF16>
 __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P) {
   cg::cluster_group cl = cg::this_cluster();
   extern __shared__ __align__(16) unsigned char smem[];
+  debug_fill_smem(smem, true);
   const Layout L = make_layout(P.nc, kBF16);
   float* xs = reinterpret_cast<float*>(smem + L.xs);
   uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem + L.cand_key);

@@ -2300,6 +2300,7 @@ __device__ __forceinline__ void row_teardown(const Params& P, int64_t row, const
 template <bool kBF16>
 __global__ void __launch_bounds__(kRT, 2) kps_prepass_kernel(const Params P) {
   extern __shared__ __align__(16) unsigned char r_smem[];
+  debug_fill_smem(r_smem, false);
   const RLayout lay = make_rlayout(P.V);
   RowSmem sm;
   sm.bitmap = reinterpret_cast<uint32_t*>(r_smem + lay.bitmap);
@@ -2367,6 +2368,7 @@ __global__ void __launch_bounds__(kRT, 2) kps_prepass_kernel(const Params P) {
 template <bool kBF16>
 __global__ void __launch_bounds__(kRT, 2) kps_row_kernel(const Params P) {
   extern __shared__ __align__(16) unsigned char r_smem[];
+  debug_fill_smem(r_smem, true);
   const RLayout lay = make_rlayout(P.V);
   RowSmem sm;
   sm.bitmap = reinterpret_cast<uint32_t*>(r_smem + lay.bitmap);
