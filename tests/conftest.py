@@ -31,3 +31,10 @@ def pytest_terminal_summary(terminalreporter):
         tr.write_line(f"{test}: {calls} comparisons, {rows} rows, {near} near, {acc} accepted")
     tot = [sum(v[i] for v in per.values()) for i in range(4)]
     tr.write_line(f"total: {tot[0]} comparisons, {tot[1]} rows, {tot[2]} near, {tot[3]} accepted")
+    # with KPS_NEAR_LOG set, every comparison is also written there, one JSON object a line
+    path = os.environ.get("KPS_NEAR_LOG")
+    if path:
+        import json
+        with open(path, "a") as f:
+            for test, label, rows, near, acc in log:
+                f.write(json.dumps({"test": test, "label": label, "rows": rows, "near": near, "accepted": acc}) + "\n")
