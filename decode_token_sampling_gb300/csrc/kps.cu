@@ -80,6 +80,7 @@ constexpr int kTopKMax = 1024;      // top-k is active for 1 <= k <= min(V, 1024
 constexpr int kCapLoc = 1024;       // candidates one CTA may hold
 constexpr int kGallCap = 2048;      // group maxima one row may have for the top-k bound
 constexpr int kGroupSplit = 8;      // groups of 128 elements split up to 8 ways (16 elements)
+constexpr int kGatherTopP = 256;    // top-k rows with at most this many survivors cut top-p on rank 0
 constexpr int kLinBins = 2048;      // linear count bins of the top-k candidate pass
 static_assert(kLinBins == 1 << 11, "the k-th bound keeps 11 bits of the key span");
 constexpr int kLinBinsP = 1024;     // linear mass bins (width 1/16 of d = max - x) of top-p-only rows
@@ -413,6 +414,25 @@ __device__ __forceinline__ uint32_t warp_incl_scan_u32(uint32_t v, int lane) {
     uint32_t w = __shfl_up_sync(kFull, v, o);
     if (lane >= o) v += w;
   }
+  return v;
+}
+
+// Block-wide sum of a u64; every thread gets the result.
+__device__ unsigned long long block_sum_u64(unsigned long long v, unsigned long long* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    v = lane < kWarps ? red[lane] : 0ull;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+    if (lane == 0) red[32] = v;
+  }
+  __syncthreads();
+  v = red[32];
+  __syncthreads();
   return v;
 }
 
@@ -1408,7 +1428,71 @@ __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P)
             }
             cand_mode = true;
             th = tk;
-            if (topp_on) {
+            bool topp_done = false;
+            if (topp_on && k <= kGatherTopP) {
+              // few survivors: rank 0 gathers the k of them from every CTA and cuts top-p
+              // over them alone by pairwise ranks (no cluster histogram, no boundary search)
+              if (threadIdx.x == 0) sh_cnt = 0u;
+              __syncthreads();
+              uint32_t mine = 0;
+              for (int i = threadIdx.x; i < ncand; i += kThreads)
+                mine += kept_by(c.cand_key[i], c.cand_idx[i], tk.key, tk.idx) ? 1u : 0u;
+              mine = __reduce_add_sync(kFull, mine);
+              if (lane == 0 && mine) atomicAdd(&sh_cnt, mine);
+              __syncthreads();
+              if (threadIdx.x == 0) push_all(cl, c.slots + kSlotFlag, rank, CS, sh_cnt);
+              cl.sync();
+              uint32_t off = 0, total = 0;
+              for (int r = 0; r < CS; ++r) {
+                const uint32_t nr = static_cast<uint32_t>(c.slots[kSlotFlag + r]);
+                off += r < rank ? nr : 0u;
+                total += nr;
+              }
+              unsigned long long* gw = reinterpret_cast<unsigned long long*>(c.fine);  // rank 0: words
+              unsigned long long* gm = gw + kGatherTopP;                                // and masses
+              if (total <= static_cast<uint32_t>(kGatherTopP)) {
+                if (threadIdx.x == 0) sh_cnt = 0u;
+                __syncthreads();
+                for (int i = threadIdx.x; i < ncand; i += kThreads) {
+                  if (!kept_by(c.cand_key[i], c.cand_idx[i], tk.key, tk.idx)) continue;
+                  const uint32_t pos = off + atomicAdd(&sh_cnt, 1u);
+                  *cl.map_shared_rank(gw + pos, 0) = order_word(c.cand_key[i], c.cand_idx[i]);
+                }
+              }
+              cl.sync();  // rank 0 holds the survivors
+              if (rank == 0) {
+                unsigned long long part = 0;
+                if (total <= static_cast<uint32_t>(kGatherTopP)) {
+                  for (uint32_t i = threadIdx.x; i < total; i += kThreads) {
+                    gm[i] = fixed_mass(softmax_weight(kfloat(static_cast<uint32_t>(gw[i] >> 32)), M));
+                    part += gm[i];
+                  }
+                }
+                const unsigned long long S = block_sum_u64(part, c.red);
+                const unsigned long long tq = ceil_mul_p(p, S);
+                if (threadIdx.x == 0) c.misc[13] = ~0ull;  // not found
+                __syncthreads();
+                if (total <= static_cast<uint32_t>(kGatherTopP) && S > 0ull) {
+                  for (uint32_t i = threadIdx.x; i < total; i += kThreads) {
+                    const unsigned long long wi = gw[i];
+                    unsigned long long excl = 0;
+                    for (uint32_t j = 0; j < total; ++j) excl += gw[j] > wi ? gm[j] : 0ull;
+                    if (excl < tq && tq <= excl + gm[i]) c.misc[13] = wi;
+                  }
+                }
+                __syncthreads();
+                if (threadIdx.x == 0) {
+                  for (int r = 0; r < CS; ++r) *cl.map_shared_rank(c.slots + kSlotTie, r) = c.misc[13];
+                }
+              }
+              cl.sync();  // every CTA holds the cut (or ~0: take the general path)
+              const unsigned long long cut = c.slots[kSlotTie];
+              if (cut != ~0ull) {
+                th = Thresh{static_cast<uint32_t>(cut >> 32), static_cast<int32_t>(~static_cast<uint32_t>(cut))};
+                topp_done = true;
+              }
+            }
+            if (topp_on && !topp_done) {
               // mass histogram of the k survivors over linear bins of (M - y)
               const float xk = kfloat(tk.key);
               const float span2 = __fsub_rn(M, xk);
