@@ -1392,10 +1392,74 @@ __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P)
         __syncthreads();
         ncand = static_cast<int>(sh_cnt);
         super_sums(hk, c.sup);
-        if (threadIdx.x == 0) push_all(cl, c.slots + kSlotFlag, rank, CS, ncand <= kCapLoc ? 1ull : 0ull);
+        if (threadIdx.x == 0) push_all(cl, c.slots + kSlotFlag, rank, CS, static_cast<unsigned long long>(ncand));
         cl.sync();
         bool lists_ok = true;
-        for (int r = 0; r < CS; ++r) lists_ok = lists_ok && c.slots[kSlotFlag + r] != 0ull;
+        uint32_t coff = 0, ctot = 0;  // this CTA's offset among the cluster's candidates, their count
+        for (int r = 0; r < CS; ++r) {
+          const uint32_t nr = static_cast<uint32_t>(c.slots[kSlotFlag + r]);
+          lists_ok = lists_ok && nr <= static_cast<uint32_t>(kCapLoc);
+          coff += r < rank ? nr : 0u;
+          ctot += nr;
+        }
+        if (lists_ok && ctot >= static_cast<uint32_t>(k) && ctot <= static_cast<uint32_t>(kGatherTopP)) {
+          // few candidates: rank 0 gathers all of them and takes the k-th (and the top-p cut
+          // over the k survivors) by pairwise ranks; no cluster histogram, no boundary search
+          unsigned long long* gw = reinterpret_cast<unsigned long long*>(c.fine);  // rank 0: words
+          unsigned long long* gm = gw + kGatherTopP;                                // masses
+          uint32_t* gr = reinterpret_cast<uint32_t*>(gw + 2 * kGatherTopP);         // ranks
+          for (int i = threadIdx.x; i < ncand; i += kThreads)
+            *cl.map_shared_rank(gw + coff + i, 0) = order_word(c.cand_key[i], c.cand_idx[i]);
+          cl.sync();  // rank 0 holds the candidates
+          if (rank == 0) {
+            if (threadIdx.x == 0) c.misc[13] = ~0ull;
+            for (uint32_t i = threadIdx.x; i < ctot; i += kThreads) {
+              const unsigned long long wi = gw[i];
+              uint32_t r = 0;
+              for (uint32_t j = 0; j < ctot; ++j) r += gw[j] > wi ? 1u : 0u;
+              gr[i] = r;
+              if (r == static_cast<uint32_t>(k) - 1u) c.misc[13] = wi;  // the k-th: the top-k cut
+            }
+            __syncthreads();
+            if (threadIdx.x == 0) c.misc[12] = c.misc[13];
+            __syncthreads();
+            if (topp_on) {
+              unsigned long long part = 0;
+              for (uint32_t i = threadIdx.x; i < ctot; i += kThreads) {
+                gm[i] = gr[i] < static_cast<uint32_t>(k)
+                            ? fixed_mass(softmax_weight(kfloat(static_cast<uint32_t>(gw[i] >> 32)), M))
+                            : 0ull;
+                part += gm[i];
+              }
+              const unsigned long long S = block_sum_u64(part, c.red);
+              const unsigned long long tq = ceil_mul_p(p, S);
+              if (S > 0ull) {
+                for (uint32_t i = threadIdx.x; i < ctot; i += kThreads) {
+                  if (gr[i] >= static_cast<uint32_t>(k)) continue;
+                  const unsigned long long wi = gw[i];
+                  unsigned long long excl = 0;
+                  for (uint32_t j = 0; j < ctot; ++j) excl += gw[j] > wi ? gm[j] : 0ull;
+                  if (excl < tq && tq <= excl + gm[i]) c.misc[12] = wi;  // the top-p cut
+                }
+              }
+              __syncthreads();
+              if (threadIdx.x == 0 && S > 0ull) c.misc[13] = c.misc[12];
+              __syncthreads();
+            }
+            if (threadIdx.x == 0) {
+              for (int r = 0; r < CS; ++r) *cl.map_shared_rank(c.slots + kSlotTie, r) = c.misc[13];
+            }
+          }
+          cl.sync();  // every CTA holds the cut
+          const unsigned long long cut = c.slots[kSlotTie];
+          th = Thresh{static_cast<uint32_t>(cut >> 32), static_cast<int32_t>(~static_cast<uint32_t>(cut))};
+          cand_mode = true;
+          if (next >= 0) {
+            issue_load(next);
+            next_issued = true;
+          }
+          fast = false;  // the general search below is not needed
+        } else {
         const Boundary bk = find_boundary(cl, c, hk, c.sup, static_cast<unsigned long long>(k), false, 0.0f);
         fast = lists_ok && bk.beta >= 0 && bk.binw <= static_cast<unsigned long long>(kSmall);
         if (fast) {
@@ -1545,6 +1609,7 @@ __global__ void __launch_bounds__(kThreads, 2) kps_sample_kernel(const Params P)
               }
             }
           }
+        }
         }
       }
       if (!cand_mode) {
