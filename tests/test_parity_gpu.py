@@ -566,3 +566,45 @@ def test_shared_topk_rows(dtype, case):
     finally:
         kps.set_kernel_policy(kps.KERNEL_AUTO)
     compare(inp, ref, gi, gf, f"shared top-k rows {case} {dtype}")
+
+
+def _spiky_rows(dtype, seed):
+    """Rows of m spikes over a background far below them, with k and m set so that the
+    number of top-k candidates a cluster collects lands on both sides of 256 (the
+    gathered-candidate paths of the cluster kernel and the histogram searches), tied spike
+    values, and top-p cuts that fall inside the spikes.  Half of each row's seen ids are
+    spike positions, so the penalty reorders them."""
+    from decode_token_sampling_gb300.workloads import f32_to_bf16_bits
+    rows = [  # (m spikes, k, p, tied values)
+        (10, 1, 0.9, None), (200, 50, 0.9, None), (256, 200, 0.5, None), (257, 256, 0.95, None),
+        (300, 100, 0.7, (6.0, 6.5, 7.0)), (600, 255, 0.3, None), (600, 300, 0.99, None), (40, 20, 0.6, (7.0,)),
+    ]
+    B, V = len(rows), 65536
+    inp = make_random(B, V, seed=seed, dtype="f32", penalty=1.3, n_seen=64)
+    rng = np.random.Generator(np.random.PCG64([0x5EED0100, seed, 7]))
+    x = rng.normal(-20.0, 0.5, (B, V)).astype(np.float32)
+    for b, (m, k, p, tied) in enumerate(rows):
+        pos = rng.choice(V, m, replace=False)
+        x[b, pos] = rng.choice(np.array(tied, np.float32), m) if tied else rng.normal(5.0, 1.0, m).astype(np.float32)
+        h = min(32, m // 2)
+        inp.seen_ids[b * 64:b * 64 + h] = pos[:h]
+        inp.top_k[b], inp.top_p[b], inp.temperature[b] = k, p, 0.8
+    inp.logits = f32_to_bf16_bits(x) if dtype == "bf16" else x
+    inp.dtype = dtype
+    inp.name = f"spiky_B{B}_V{V}"
+    return inp
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_spiky_rows_around_the_candidate_gather(dtype, kernel):
+    """Top-k rows whose candidates number from a handful to several hundred: with at most
+    256 in the cluster, rank 0 gathers them and ranks them pairwise for the k-th and the
+    top-p cut; above that, the histogram searches run (and rank 0 still cuts top-p over
+    the gathered survivors when k <= 256).  Against the oracle, with filtered logits."""
+    import decode_token_sampling_gb300 as kps
+    inp = _spiky_rows(dtype, seed=171)
+    ref = oracle.sample(inp)
+    gi, gf = run_gpu(inp)
+    if kernel == "cluster":
+        assert kps.last_kernel() == "kps_sample_kernel"
+    compare(inp, ref, gi, gf, f"spiky rows {dtype}")
