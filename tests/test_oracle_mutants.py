@@ -40,6 +40,10 @@ MUTANTS = [
     ("Philox Weyl increment", "k0 += 0x9E3779B9u;", "k0 += 0x9E3779B1u;"),
     ("finished rows keep their token", "if (finished[b]) idx[b] = eos;", ";"),
     ("seen append to the wrong bit", "1u << (idx[b] % 32)", "1u << ((idx[b] + 1) % 32)"),
+    ("bf16 widened one bit short", "static_cast<uint32_t>(h) << 16", "static_cast<uint32_t>(h) << 15"),
+    ("non-positive temperature divides", "t.greedy = !(T > 0.0f) || std::isinf(T);", "t.greedy = false;"),
+    ("top-k keeps one more", "    nK = k;\n", "    nK = std::min<int64_t>(V, k + 1);\n"),
+    ("sampling off takes the last kept", "return RowResult{order[0], nP,", "return RowResult{order[nP - 1], nP,"),
 ]
 
 
