@@ -44,6 +44,10 @@ MUTANTS = [
     ("non-positive temperature divides", "t.greedy = !(T > 0.0f) || std::isinf(T);", "t.greedy = false;"),
     ("top-k keeps one more", "    nK = k;\n", "    nK = std::min<int64_t>(V, k + 1);\n"),
     ("sampling off takes the last kept", "return RowResult{order[0], nP,", "return RowResult{order[nP - 1], nP,"),
+    ("top-p drops the crossing element", "while (nP < nK && c < target) {", "while (nP < nK && c + e[nP] < target) {"),
+    ("race over the top-k set", "for (int64_t i = 0; i < nP; ++i) {\n    int64_t v = order[i];",
+     "for (int64_t i = 0; i < nK; ++i) {\n    int64_t v = order[i];"),
+    ("NaN race scores compete", "if (std::isnan(r)) continue;", ";"),
 ]
 
 

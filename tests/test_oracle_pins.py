@@ -157,6 +157,8 @@ def test_brute_force_tiny_rows(seed):
         p = float(np.float32(rng.choice([0.0, -0.5, 0.3, 0.6, 0.9, 0.999, 1.0, 1.5])))
         T = float(np.float32(rng.choice([1.0, 0.7, 1.3, 0.0, -1.0])))
         q = rng.exponential(1.0, V).astype(np.float32)
+        if rng.random() < 0.25:  # NaN draws: their race scores take no part
+            q[rng.random(V) < 0.4] = np.nan
         seen = rng.integers(-1, V + 1, 4).tolist() if rng.random() < 0.5 else None
         pen = 1.3
         r = oracle.sample_arrays(x[None], "f32", [k], [p], [T], q[None], 1e-20, True,
@@ -174,6 +176,21 @@ def test_brute_force_tiny_rows(seed):
         for v in want_P:
             if np.isfinite(xt[v]):
                 assert r["filtered"][0][v] == xt[v]
+
+
+def test_nan_draws_take_no_part_in_the_race():
+    """A NaN draw makes its token's race score NaN, and NaN scores are ignored: the best
+    of the others wins, and with every score NaN the first token of the order is chosen
+    (the reading of the race's argmax for NaN scores).  Expected values from brute_row."""
+    x = np.array([3.0, 2.0, 1.0, 0.0], np.float32)
+    nan = np.float32(np.nan)
+    cases = [[nan, 1.0, 1.0, 1.0], [1.0, nan, 0.01, 1.0], [nan, nan, nan, nan], [nan, nan, nan, 0.5]]
+    for q in cases:
+        q = np.array(q, np.float32)
+        r = run1(x.tolist(), top_k=0, top_p=1.0, temperature=1.0, q=q.tolist())
+        want, _, _ = brute_row(x, 0, 1.0, 1.0, q, 1e-20, None, 0.0)
+        assert r["idx"][0] == want, (q, r["idx"][0], want)
+    assert [run1(x.tolist(), q=c)["idx"][0] for c in cases] == [1, 2, 0, 3]
 
 
 # ----------------------------------------------------------------------------------------------
