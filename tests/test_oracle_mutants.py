@@ -48,6 +48,12 @@ MUTANTS = [
     ("race over the top-k set", "for (int64_t i = 0; i < nP; ++i) {\n    int64_t v = order[i];",
      "for (int64_t i = 0; i < nK; ++i) {\n    int64_t v = order[i];"),
     ("NaN race scores compete", "if (std::isnan(r)) continue;", ";"),
+    ("top-k set left unsorted", "std::sort(order.begin(), order.begin() + nK, before);", ";"),
+    ("greedy rows keep the nucleus", "if (greedy || p <= 0.0f) {", "if (p <= 0.0f) {"),
+    ("EOS token does not finish its row", "if (idx[b] == eos) finished[b] = 1;", ";"),
+    ("finished rows counted as left", "if (!finished[b]) ++left;", "++left;"),
+    ("seen bits row stride off by one", "bits[b * W + v / 32] >> (v % 32)", "bits[b * (W - 1) + v / 32] >> (v % 32)"),
+    ("draw takes the next word", "const uint32_t w = c[v & 3];", "const uint32_t w = c[(v + 1) & 3];"),
 ]
 
 
